@@ -1,0 +1,101 @@
+/*
+ * lssar_attn_fwd.h -- C ABI of the GB300 (sm_103a) causal LSSAR attention forward.
+ *
+ * The operation is the attention forward defined in the papernotes.org notes on
+ * "Softplus Attention with Re-weighting Boosts Length Extrapolation in Large
+ * Language Models" (arXiv 2501.13428):
+ *
+ *   Key design 1 (LSSA): q_i <- q_i/||q_i||_2, k_j <- k_j/||k_j||_2,
+ *       A_ij = Softplus(ln d * ln i * q_i.k_j) for j <= i (0 above the diagonal,
+ *       a multiplicative mask applied after the Softplus), then each row of A is
+ *       divided by its sum.  i is the 1-based row index (tokens attended).
+ *   Key design 2 (re-weighting): A_ij <- max(i*A_ij - O_i, 0)^p with O_i = 0 for
+ *       rows 1..3 and 1 otherwise, then each row is divided by its sum again.
+ *   The output row i is sum_j A_ij v_j.
+ *   Background (softmax mode): A = Softmax(q.k^T / sqrt(d) + causal -inf mask).
+ *
+ * A re-weighted row whose entries are all zero (possible only when the LSSA
+ * row is exactly uniform) is 0/0 in the notes; this library returns the
+ * uniform prefix mean for it.  Norms are clamped at 1e-12.
+ *
+ * Conventions shared by every entry point:
+ *   - q, k, v, out are DEVICE pointers to bfloat16 tensors of shape
+ *     [B, H, L, d], contiguous (d fastest), each 16-byte aligned.  The caller
+ *     owns them; out must not overlap q, k or v.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and return
+ *     once the work is enqueued.  Errors in the arguments are reported before
+ *     anything is launched; nothing is written to `out` in that case.
+ *   - Temporary device memory is taken stream-ordered from a memory pool owned
+ *     by the library and released stream-ordered on the same stream.
+ *   - Thread-safe: no mutable global state besides the lazily created pool
+ *     (guarded) and the device error word (see lssar_device_error_word).
+ */
+#ifndef LSSAR_ATTN_FWD_H
+#define LSSAR_ATTN_FWD_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t. */
+typedef struct CUstream_st *cudaStream_t;
+
+typedef enum {
+    LSSAR_MODE_SOFTMAX = 0, /* Softmax(q.k^T/sqrt(d)) on raw q, k (Background)       */
+    LSSAR_MODE_LSSA = 1,    /* Key design 1 only                                      */
+    LSSAR_MODE_LSSAR = 2    /* Key design 1 followed by Key design 2                  */
+} lssar_mode_t;
+
+typedef enum {
+    LSSAR_OK = 0,
+    LSSAR_ERR_NULL = -1,    /* a tensor pointer is NULL                               */
+    LSSAR_ERR_SHAPE = -2,   /* B, H or L < 1, or B*H*L*d beyond 2^40                  */
+    LSSAR_ERR_HEADDIM = -3, /* d is not 64 or 128                                     */
+    LSSAR_ERR_P = -4,       /* LSSAR mode with p < 1 or p > 1024                      */
+    LSSAR_ERR_MODE = -5,    /* unknown mode                                           */
+    LSSAR_ERR_ALIGN = -6,   /* a pointer is not 16-byte aligned                       */
+    LSSAR_ERR_CUDA = -7,    /* a CUDA call failed (launch, pool allocation, ...)      */
+    LSSAR_ERR_ALIAS = -8    /* out overlaps q, k or v                                 */
+} lssar_status_t;
+
+/*
+ * Causal attention forward, computed by the tensor-core (tcgen05/TMEM/TMA)
+ * kernel for sm_103a.
+ *   q, k, v : [B, H, L, d] bfloat16, device, read only.
+ *   out     : [B, H, L, d] bfloat16, device, written (row i of head (b, h)).
+ *   p       : integer exponent of the re-weighting (LSSAR mode only, 1..1024;
+ *             ignored in the other modes).
+ *   mode    : lssar_mode_t.
+ * Returns LSSAR_OK or a negative lssar_status_t.
+ */
+int lssar_attn_fwd(const void *q, const void *k, const void *v, void *out,
+                   int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
+
+/*
+ * Same operation and contract as lssar_attn_fwd, computed by a plain CUDA-core
+ * kernel (one warp per query row, fp32 throughout, accurate libm softplus).
+ * It is a second, independent GPU implementation kept for cross-checking the
+ * tensor-core kernel; it is not tuned for speed.
+ */
+int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out,
+                        int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *lssar_status_string(int status);
+
+/*
+ * Reads and clears the device error word of the current device: 0 when no
+ * kernel of this library has hit a bounded wait since the last call, else a
+ * code (1-based pipeline stage) of the first wait that gave up.  Synchronises
+ * the current device.  Returns LSSAR_OK or LSSAR_ERR_CUDA.
+ */
+int lssar_device_error_word(unsigned int *word);
+
+/* Version of this ABI: major * 10000 + minor * 100 + patch. */
+int lssar_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LSSAR_ATTN_FWD_H */

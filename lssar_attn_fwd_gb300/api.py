@@ -1,0 +1,125 @@
+"""ctypes binding of liblssar_attn_fwd.so (argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only checks tensor metadata, takes raw device pointers and the current CUDA
+stream from PyTorch and calls the C ABI declared in
+``include/lssar_attn_fwd.h``.  There is no fallback: if the library is not
+built, or a call fails, an exception is raised.
+"""
+
+import ctypes
+import os
+
+from .inputs import MODE_LSSA, MODE_LSSAR, MODE_SOFTMAX  # noqa: F401
+
+_LIB = None
+
+_EXPORTS = (
+    "lssar_attn_fwd",
+    "lssar_attn_fwd_simt",
+    "lssar_status_string",
+    "lssar_device_error_word",
+    "lssar_abi_version",
+)
+
+
+class LssarError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"lssar status {status}: {message}")
+        self.status = status
+
+
+def lib_path():
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "liblssar_attn_fwd.so")
+
+
+def load_library():
+    """Loads the shared library (once).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m lssar_attn_fwd_gb300.build` "
+            "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    fwd_args = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
+    for name in ("lssar_attn_fwd", "lssar_attn_fwd_simt"):
+        fn = getattr(lib, name)
+        fn.argtypes = fwd_args
+        fn.restype = ctypes.c_int
+    lib.lssar_status_string.argtypes = [ctypes.c_int]
+    lib.lssar_status_string.restype = ctypes.c_char_p
+    lib.lssar_device_error_word.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    lib.lssar_device_error_word.restype = ctypes.c_int
+    lib.lssar_abi_version.argtypes = []
+    lib.lssar_abi_version.restype = ctypes.c_int
+    _LIB = lib
+    return lib
+
+
+def status_string(status):
+    return load_library().lssar_status_string(int(status)).decode()
+
+
+def call_raw(name, q_ptr, k_ptr, v_ptr, out_ptr, B, H, L, d, p, mode, stream_handle):
+    """Calls a forward entry point with raw integer pointers; returns the status."""
+    fn = getattr(load_library(), name)
+    return fn(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+              ctypes.c_void_p(out_ptr), int(B), int(H), int(L), int(d), int(p), int(mode),
+              ctypes.c_void_p(stream_handle))
+
+
+def _check(status):
+    if status != 0:
+        raise LssarError(status, status_string(status))
+
+
+def _forward(name, q, k, v, p, mode, out, stream):
+    import torch
+
+    for t in (q, k, v):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("q, k, v must be torch tensors")
+        if t.device.type != "cuda" or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bfloat16 CUDA tensors")
+        if t.dim() != 4 or t.shape != q.shape:
+            raise ValueError("q, k, v must share one [B, H, L, d] shape")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    B, H, L, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    elif (out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous()
+          or out.device != q.device):
+        raise ValueError("out must be a contiguous bfloat16 tensor shaped like q on q's device")
+    with torch.cuda.device(q.device):
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        _check(call_raw(name, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                        B, H, L, d, p, mode, handle))
+    return out
+
+
+def lssar_attn_fwd(q, k, v, p=3, mode=MODE_LSSAR, out=None, stream=None):
+    """Causal LSSAR / LSSA / softmax attention forward on the tensor-core kernel.
+
+    q, k, v: contiguous bf16 CUDA tensors [B, H, L, d] (d = 64 or 128).
+    p: re-weighting exponent (LSSAR mode).  mode: 0 softmax, 1 LSSA, 2 LSSAR.
+    Runs asynchronously on ``stream`` (default: the current stream).
+    """
+    return _forward("lssar_attn_fwd", q, k, v, p, mode, out, stream)
+
+
+def lssar_attn_fwd_simt(q, k, v, p=3, mode=MODE_LSSAR, out=None, stream=None):
+    """Same operation on the plain CUDA-core kernel (cross-check only)."""
+    return _forward("lssar_attn_fwd_simt", q, k, v, p, mode, out, stream)
+
+
+def device_error_word():
+    """Reads and clears the device error word (synchronises the device)."""
+    w = ctypes.c_uint(0)
+    _check(load_library().lssar_device_error_word(ctypes.byref(w)))
+    return w.value

@@ -1,0 +1,124 @@
+// C ABI of liblssar_attn_fwd.so: argument validation, the stream-ordered
+// scratch pool and dispatch to the kernels.  The declarations and the full
+// contract are in include/lssar_attn_fwd.h.
+#include <cstdint>
+#include <mutex>
+
+#include "lssar_attn_fwd.h"
+#include "lssar_internal.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxP = 1024;
+
+bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const auto x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Pure host checks; never touches the CUDA runtime.
+int validate(const void *q, const void *k, const void *v, void *out, int B, int H, int L, int d,
+             int p, int mode, lssar::Problem *pr) {
+    if (!q || !k || !v || !out) return LSSAR_ERR_NULL;
+    if (mode != LSSAR_MODE_SOFTMAX && mode != LSSAR_MODE_LSSA && mode != LSSAR_MODE_LSSAR)
+        return LSSAR_ERR_MODE;
+    if (B < 1 || H < 1 || L < 1) return LSSAR_ERR_SHAPE;
+    if (d != 64 && d != 128) return LSSAR_ERR_HEADDIM;
+    const unsigned long long elems = (unsigned long long)B * H * L * d;
+    if (elems > (1ULL << 40)) return LSSAR_ERR_SHAPE;
+    if (mode == LSSAR_MODE_LSSAR && (p < 1 || p > kMaxP)) return LSSAR_ERR_P;
+    for (const void *ptr : {q, k, v, static_cast<const void *>(out)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15u) return LSSAR_ERR_ALIGN;
+    const size_t bytes = (size_t)elems * 2;
+    if (ranges_overlap(out, bytes, q, bytes) || ranges_overlap(out, bytes, k, bytes) ||
+        ranges_overlap(out, bytes, v, bytes))
+        return LSSAR_ERR_ALIAS;
+    *pr = lssar::Problem{q, k, v, out, B, H, L, d, mode == LSSAR_MODE_LSSAR ? p : 1, mode};
+    return LSSAR_OK;
+}
+
+// One memory pool per device, created on first use and kept for the life of
+// the process.  Its release threshold is raised so that freed scratch stays
+// cached in the pool instead of going back to the driver at every sync.
+std::mutex g_pool_mutex;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+
+cudaError_t device_pool(cudaMemPool_t *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool;
+        e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return e;
+        }
+        g_pools[dev] = pool;
+    }
+    *out = g_pools[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lssar_attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+                   int d, int p, int mode, cudaStream_t stream) {
+    lssar::Problem pr;
+    const int st = validate(q, k, v, out, B, H, L, d, p, mode, &pr);
+    if (st != LSSAR_OK) return st;
+    const size_t ws_bytes = lssar::tc_workspace_bytes(pr);
+    void *ws = nullptr;
+    if (ws_bytes) {
+        cudaMemPool_t pool;
+        if (device_pool(&pool) != cudaSuccess) return LSSAR_ERR_CUDA;
+        if (cudaMallocFromPoolAsync(&ws, ws_bytes, pool, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    }
+    const cudaError_t e = lssar::launch_tc(pr, ws, stream);
+    if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
+}
+
+int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out, int B, int H,
+                        int L, int d, int p, int mode, cudaStream_t stream) {
+    lssar::Problem pr;
+    const int st = validate(q, k, v, out, B, H, L, d, p, mode, &pr);
+    if (st != LSSAR_OK) return st;
+    return lssar::launch_simt(pr, stream) == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
+}
+
+const char *lssar_status_string(int status) {
+    switch (status) {
+        case LSSAR_OK: return "ok";
+        case LSSAR_ERR_NULL: return "null tensor pointer";
+        case LSSAR_ERR_SHAPE: return "invalid shape (B, H, L >= 1 and B*H*L*d <= 2^40)";
+        case LSSAR_ERR_HEADDIM: return "head dimension must be 64 or 128";
+        case LSSAR_ERR_P: return "LSSAR exponent p must be in 1..1024";
+        case LSSAR_ERR_MODE: return "unknown mode";
+        case LSSAR_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+        case LSSAR_ERR_CUDA: return "CUDA error";
+        case LSSAR_ERR_ALIAS: return "out overlaps q, k or v";
+        default: return "unknown status";
+    }
+}
+
+int lssar_device_error_word(unsigned int *word) {
+    if (!word) return LSSAR_ERR_NULL;
+    return lssar::read_and_clear_error_word(word) == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
+}
+
+int lssar_abi_version(void) { return 10000; }
+
+}  // extern "C"

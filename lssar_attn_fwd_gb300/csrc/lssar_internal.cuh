@@ -1,0 +1,31 @@
+// Internal declarations shared by the translation units of liblssar_attn_fwd.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace lssar {
+
+enum Mode : int { kSoftmax = 0, kLssa = 1, kLssar = 2 };
+
+// Problem description after validation.  Tensors are [B, H, L, d] bf16.
+struct Problem {
+    const void *q;
+    const void *k;
+    const void *v;
+    void *out;
+    int B, H, L, d, p, mode;
+};
+
+// Plain CUDA-core kernel (one warp per query row).  Returns a cudaError_t.
+cudaError_t launch_simt(const Problem &pr, cudaStream_t stream);
+
+// Tensor-core path (tcgen05 + TMEM + TMA).  `ws` is device scratch of at
+// least tc_workspace_bytes(pr) bytes, 256-byte aligned.
+size_t tc_workspace_bytes(const Problem &pr);
+cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream);
+
+// Reads and clears the device error word of the current device.
+cudaError_t read_and_clear_error_word(unsigned int *word);
+
+}  // namespace lssar

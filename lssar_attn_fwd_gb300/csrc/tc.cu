@@ -1,0 +1,201 @@
+// Host side of the tensor-core path: the row-normalisation prologue, TMA
+// tensor maps, template dispatch and launch, and the device error word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tc_kernel.cuh"
+
+namespace lssar {
+
+namespace {
+
+__device__ unsigned g_error_word;
+
+// q_i / max(|q_i|, 1e-12) and k_j / max(|k_j|, 1e-12) rounded to fp16 (Key
+// design 1 of the notes: rows are L2-normalised before the score product).
+// Each row is handled by D/8 consecutive threads, 8 elements each.
+template <int D>
+__global__ void __launch_bounds__(256) normalize_rows_fp16(const __nv_bfloat16 *__restrict__ q,
+                                                           const __nv_bfloat16 *__restrict__ k,
+                                                           __half *__restrict__ qh,
+                                                           __half *__restrict__ kh,
+                                                           long long rows) {
+    constexpr int G = D / 8;
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long r = tid / G;
+    const int part = (int)(tid % G);
+    const bool live = r < 2 * rows;
+    const bool is_k = r >= rows;
+    const long long rr = is_k ? r - rows : r;
+    float x[8];
+    float ss = 0.f;
+    if (live) {
+        const __nv_bfloat16 *src = (is_k ? k : q) + rr * D + part * 8;
+        const uint4 u = *reinterpret_cast<const uint4 *>(src);
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h[e]);
+            x[2 * e] = f.x;
+            x[2 * e + 1] = f.y;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+    }
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (!live) return;
+    const float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+    uint4 u;
+    __half2 *h = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(x[2 * e] * inv, x[2 * e + 1] * inv);
+    __half *dst = (is_k ? kh : qh) + rr * D + part * 8;
+    *reinterpret_cast<uint4 *>(dst) = u;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [BH, L, D] tensor of 16-bit elements, boxes of 64 elements x 128 rows,
+// 128-byte swizzle; rows past L read as zero.
+bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int BH, int L, int D) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)L * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)tc::kBM, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int MODE, int PK>
+cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                          const tc::Params &prm, int grid, cudaStream_t stream) {
+    auto kern = tc::lssar_tc_kernel<D, MODE, PK>;
+    constexpr int smem = tc::Cfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, tc::kThreads, smem, stream>>>(mq, mk, mv, prm);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch(const Problem &pr, const CUtensorMap &mq, const CUtensorMap &mk,
+                     const CUtensorMap &mv, const tc::Params &prm, int grid, cudaStream_t s) {
+    switch (pr.mode) {
+        case kSoftmax: return launch_kernel<D, kSoftmax, 0>(mq, mk, mv, prm, grid, s);
+        case kLssa: return launch_kernel<D, kLssa, 0>(mq, mk, mv, prm, grid, s);
+        default:
+            switch (pr.p) {
+                case 1: return launch_kernel<D, kLssar, 1>(mq, mk, mv, prm, grid, s);
+                case 2: return launch_kernel<D, kLssar, 2>(mq, mk, mv, prm, grid, s);
+                case 3: return launch_kernel<D, kLssar, 3>(mq, mk, mv, prm, grid, s);
+                case 15: return launch_kernel<D, kLssar, 15>(mq, mk, mv, prm, grid, s);
+                default: return launch_kernel<D, kLssar, 0>(mq, mk, mv, prm, grid, s);
+            }
+    }
+}
+
+std::mutex g_sym_mutex;
+unsigned *g_err_ptr[64] = {};
+
+cudaError_t error_word_ptr(unsigned **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_sym_mutex);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_error_word);
+        if (e != cudaSuccess) return e;
+        g_err_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_err_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t tc_workspace_bytes(const Problem &pr) {
+    if (pr.mode == kSoftmax) return 0;
+    // normalised q and k in fp16, 256-byte aligned halves
+    const size_t half = ((size_t)pr.B * pr.H * pr.L * pr.d * 2 + 255) & ~(size_t)255;
+    return 2 * half;
+}
+
+cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream) {
+    const int BH = pr.B * pr.H;
+    const long long rows = (long long)BH * pr.L;
+    const void *qsrc = pr.q, *ksrc = pr.k;
+    CUtensorMapDataType qk_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (pr.mode != kSoftmax) {
+        const size_t half = tc_workspace_bytes(pr) / 2;
+        __half *qh = static_cast<__half *>(ws);
+        __half *kh = reinterpret_cast<__half *>(static_cast<char *>(ws) + half);
+        const long long threads = 2 * rows * (pr.d / 8);
+        const long long blocks = (threads + 255) / 256;
+        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
+        const auto *k = static_cast<const __nv_bfloat16 *>(pr.k);
+        if (pr.d == 64)
+            normalize_rows_fp16<64><<<(unsigned)blocks, 256, 0, stream>>>(q, k, qh, kh, rows);
+        else
+            normalize_rows_fp16<128><<<(unsigned)blocks, 256, 0, stream>>>(q, k, qh, kh, rows);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        qsrc = qh;
+        ksrc = kh;
+        qk_type = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    }
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, qsrc, qk_type, BH, pr.L, pr.d) || !make_map(&mk, ksrc, qk_type, BH, pr.L, pr.d) ||
+        !make_map(&mv, pr.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, BH, pr.L, pr.d))
+        return cudaErrorInvalidValue;
+
+    tc::Params prm;
+    prm.BH = BH;
+    prm.L = pr.L;
+    prm.n_qtiles = (pr.L + tc::kBM - 1) / tc::kBM;
+    prm.n_pairs = (prm.n_qtiles + 1) / 2;
+    prm.n_items = BH * prm.n_pairs;
+    prm.ln_d = logf((float)pr.d);
+    prm.p = pr.p;
+    prm.out = static_cast<__nv_bfloat16 *>(pr.out);
+    cudaError_t e = error_word_ptr(&prm.err);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int grid = prm.n_items < sms ? prm.n_items : sms;
+    return pr.d == 64 ? dispatch<64>(pr, mq, mk, mv, prm, grid, stream)
+                      : dispatch<128>(pr, mq, mk, mv, prm, grid, stream);
+}
+
+cudaError_t read_and_clear_error_word(unsigned int *word) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(word, g_error_word, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned));
+}
+
+}  // namespace lssar

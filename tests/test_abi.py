@@ -1,0 +1,95 @@
+"""Host-only checks of the C ABI: the library builds, loads, exports every
+declared symbol, and rejects invalid arguments before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+# Fake, far-apart, 16-byte aligned addresses: only ever passed together with
+# at least one invalid argument, so nothing is dereferenced or launched.
+Q, K, V, OUT = 1 << 32, 2 << 32, 3 << 32, 4 << 32
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from lssar_attn_fwd_gb300 import build
+    from lssar_attn_fwd_gb300 import api
+    build.build()
+    return api.load_library()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(HEADER_DIR):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(lssar_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    assert "lssar_attn_fwd" in names and "lssar_status_string" in names
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared but not exported"
+
+
+def test_abi_version(lib):
+    assert lib.lssar_abi_version() >= 10000
+
+
+def call(lib, name="lssar_attn_fwd", q=Q, k=K, v=V, out=OUT, B=1, H=1, L=16, d=64, p=3, mode=2):
+    from lssar_attn_fwd_gb300.api import call_raw
+    return call_raw(name, q, k, v, out, B, H, L, d, p, mode, 0)
+
+
+@pytest.mark.parametrize("name", ["lssar_attn_fwd", "lssar_attn_fwd_simt"])
+def test_invalid_arguments(lib, name):
+    assert call(lib, name, q=0) == -1
+    assert call(lib, name, out=0) == -1
+    assert call(lib, name, mode=3) == -5
+    assert call(lib, name, mode=-1) == -5
+    assert call(lib, name, B=0) == -2
+    assert call(lib, name, H=-1) == -2
+    assert call(lib, name, L=0) == -2
+    assert call(lib, name, B=1 << 20, H=1 << 20, L=1 << 10, d=64) == -2
+    assert call(lib, name, d=96) == -3
+    assert call(lib, name, d=256) == -3
+    assert call(lib, name, p=0) == -4
+    assert call(lib, name, p=1025) == -4
+    assert call(lib, name, q=Q + 8) == -6
+    assert call(lib, name, v=V + 2) == -6
+    assert call(lib, name, out=Q + 1024) == -8   # out overlaps q
+    assert call(lib, name, out=K - 1024) == -8   # out's range runs into k
+
+
+def test_status_strings(lib):
+    from lssar_attn_fwd_gb300.api import status_string
+    assert status_string(0) == "ok"
+    assert "64 or 128" in status_string(-3)
+    assert status_string(-99) == "unknown status"
+
+
+def test_binding_rejects_non_cuda_tensors():
+    torch = pytest.importorskip("torch")
+    from lssar_attn_fwd_gb300.api import lssar_attn_fwd
+    x = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16)
+    with pytest.raises((ValueError, RuntimeError)):
+        lssar_attn_fwd(x, x, x)
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    from lssar_attn_fwd_gb300 import api
+    monkeypatch.setattr(api, "_LIB", None)
+    monkeypatch.setattr(api, "lib_path", lambda: "/nonexistent/liblssar_attn_fwd.so")
+    with pytest.raises(RuntimeError, match="no fallback"):
+        api.load_library()

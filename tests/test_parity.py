@@ -1,0 +1,198 @@
+"""GPU parity: the tensor-core kernel (through the C ABI) against the float64
+oracle on the same seeded bf16 inputs.
+
+Tolerance (max abs error of the bf16 output against the float64 oracle):
+2e-2 for LSSA, softmax and LSSAR with p <= 3; 5e-2 for p >= 15.  The
+budget is dominated by the bf16 rounding of the output (up to 1.6e-2 for
+|out| in [4, 8)), bf16 rounding of the weights fed to the tensor core, and
+fp16 rounding of the normalised q, k in the score product.
+"""
+
+import numpy as np
+import pytest
+
+from lssar_attn_fwd_gb300.inputs import (
+    MODE_LSSA, MODE_LSSAR, MODE_SOFTMAX, WORKLOADS, bf16_bits_to_f64, make_qkv, needle_targets)
+from oracle import attention_forward
+
+pytestmark = pytest.mark.gpu
+
+
+def tol(mode, p):
+    return 5e-2 if (mode == MODE_LSSAR and p >= 15) else 2e-2
+
+
+@pytest.fixture(scope="module")
+def torch_mod():
+    import torch
+    from lssar_attn_fwd_gb300 import api, build
+    build.build()
+    api.load_library()
+    return torch
+
+
+def to_dev(torch, bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def run(torch, qb, kb, vb, p, mode, impl="tc"):
+    from lssar_attn_fwd_gb300 import api
+    q, k, v = (to_dev(torch, t) for t in (qb, kb, vb))
+    fn = api.lssar_attn_fwd if impl == "tc" else api.lssar_attn_fwd_simt
+    out = fn(q, k, v, p=p, mode=mode)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def check_error_word():
+    from lssar_attn_fwd_gb300 import api
+    assert api.device_error_word() == 0
+
+
+MODES = [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_LSSAR, 1), (MODE_LSSAR, 2), (MODE_LSSAR, 7),
+         (MODE_LSSA, 1), (MODE_SOFTMAX, 1)]
+
+
+@pytest.mark.parametrize("mode,p", MODES)
+def test_tiny_all_modes(torch_mod, mode, p):
+    w = WORKLOADS["tiny"]
+    qb, kb, vb = make_qkv(*w.shape, seed=0)
+    got = run(torch_mod, qb, kb, vb, p, mode)
+    ref = attention_forward(*(bf16_bits_to_f64(t) for t in (qb, kb, vb)), mode, p)
+    err = np.abs(got - ref).max()
+    assert err <= tol(mode, p), err
+    check_error_word()
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 5, 127, 129, 200, 255, 256, 257, 300, 513])
+@pytest.mark.parametrize("d", [64, 128])
+def test_ragged_lengths(torch_mod, L, d):
+    qb, kb, vb = make_qkv(2, 2, L, d, seed=L + d)
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    for mode, p in [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_LSSA, 1), (MODE_SOFTMAX, 1)]:
+        got = run(torch_mod, qb, kb, vb, p, mode)
+        ref = attention_forward(qf, kf, vf, mode, p)
+        err = np.abs(got - ref).max()
+        assert err <= tol(mode, p), (mode, p, err)
+    check_error_word()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_multi_pair_full_check(torch_mod, d):
+    # several Q-tile pairs per head, a ragged tail, more items than SMs
+    B, H, L = 3, 60, 700
+    qb, kb, vb = make_qkv(B, H, L, d, seed=d)
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    heads = [(0, 0), (1, 17), (2, 59)]
+    for mode, p in [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_SOFTMAX, 1), (MODE_LSSA, 1)]:
+        got = run(torch_mod, qb, kb, vb, p, mode)
+        for b, h in heads:
+            ref = attention_forward(qf[b, h], kf[b, h], vf[b, h], mode, p)
+            err = np.abs(got[b, h] - ref).max()
+            assert err <= tol(mode, p), (mode, p, b, h, err)
+    check_error_word()
+
+
+def sample_rows(L, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [1, 2, 3, 4, 5, 127, 128, 129, 256, 257, L // 2, L - 1, L]
+    return np.unique(np.clip(np.concatenate([fixed, rng.integers(1, L + 1, 24)]), 1, L))
+
+
+@pytest.mark.parametrize("name", ["gpt2", "extrap", "needle", "wide"])
+def test_full_size_sampled_rows(torch_mod, name):
+    w = WORKLOADS[name]
+    qb, kb, vb = make_qkv(*w.shape, seed=0, structure=w.structure)
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    rows = sample_rows(w.L, seed=1)
+    heads = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 2)]
+    for mode, p in w.runs:
+        got = run(torch_mod, qb, kb, vb, p, mode)
+        assert np.isfinite(got).all()
+        for b, h in heads:
+            ref = attention_forward(qf[b, h], kf[b, h], vf[b, h], mode, p, rows=rows)
+            err = np.abs(got[b, h, rows - 1] - ref).max()
+            assert err <= tol(mode, p), (name, mode, p, b, h, err)
+    check_error_word()
+
+
+def test_rows_sum_to_one_full_size(torch_mod):
+    # V = ones: every mode ends in an L1 normalisation, so out == 1.
+    w = WORKLOADS["extrap"]
+    qb, kb, _ = make_qkv(*w.shape, seed=2)
+    ones = np.full(w.shape, 0x3F80, dtype=np.uint16)   # bf16 1.0
+    for mode, p in [(MODE_LSSAR, 15), (MODE_LSSAR, 3), (MODE_LSSA, 1), (MODE_SOFTMAX, 1)]:
+        got = run(torch_mod, qb, kb, ones, p, mode)
+        assert np.abs(got - 1.0).max() <= 1e-2, mode
+
+
+def test_first_row_is_first_value(torch_mod):
+    qb, kb, vb = make_qkv(2, 3, 384, 64, seed=5)
+    vf = bf16_bits_to_f64(vb)
+    for mode, p in [(MODE_LSSAR, 15), (MODE_LSSA, 1), (MODE_SOFTMAX, 1)]:
+        got = run(torch_mod, qb, kb, vb, p, mode)
+        np.testing.assert_array_equal(got[:, :, 0], vf[:, :, 0])
+
+
+def test_identical_keys_give_prefix_mean(torch_mod):
+    # Uniform scores: LSSA weights 1/i; LSSAR rows from 4 on are all-zero
+    # (0/0) re-weighted rows, read as the uniform prefix mean.
+    B, H, L, d = 1, 2, 600, 64
+    qb, kb, vb = make_qkv(B, H, L, d, seed=6)
+    kb = np.broadcast_to(kb[:, :, :1], kb.shape).copy()
+    vf = bf16_bits_to_f64(vb)
+    mean = np.cumsum(vf, axis=2) / np.arange(1, L + 1)[None, None, :, None]
+    for mode, p in [(MODE_LSSA, 1), (MODE_LSSAR, 3), (MODE_LSSAR, 15)]:
+        got = run(torch_mod, qb, kb, vb, p, mode)
+        assert np.abs(got - mean).max() <= 2e-2, mode
+
+
+def test_needle_large_p_is_argmax(torch_mod):
+    # p = 64 (generic power path): the weight concentrates on the needle key.
+    B, H, L, d = 1, 2, 1024, 64
+    qb, kb, vb = make_qkv(B, H, L, d, seed=3, structure="needle")
+    j = needle_targets(B, H, L, d, seed=3)
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    got = run(torch_mod, qb, kb, vb, 64, MODE_LSSAR)
+    rows = sample_rows(L, seed=4)
+    for h in range(H):
+        ref = attention_forward(qf[0, h], kf[0, h], vf[0, h], MODE_LSSAR, 64, rows=rows)
+        assert np.abs(got[0, h, rows - 1] - ref).max() <= 5e-2
+    picked = np.take_along_axis(vf, (j - 1)[..., None].repeat(d, -1), axis=2)
+    close = np.abs(got - picked).max(axis=-1) < 5e-2
+    assert close[:, :, 64:].mean() > 0.95
+
+
+def test_tc_matches_simt_full_size(torch_mod):
+    # Consistency between the two GPU implementations on every row (an extra
+    # check beside the oracle parity above).
+    w = WORKLOADS["gpt2"]
+    qb, kb, vb = make_qkv(*w.shape, seed=7)
+    for mode, p in w.runs:
+        a = run(torch_mod, qb, kb, vb, p, mode, "tc")
+        b = run(torch_mod, qb, kb, vb, p, mode, "simt")
+        assert np.abs(a - b).max() <= 2 * tol(mode, p)
+
+
+def test_simt_matches_oracle(torch_mod):
+    qb, kb, vb = make_qkv(1, 2, 300, 128, seed=8)
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    for mode, p in [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_LSSA, 1), (MODE_SOFTMAX, 1)]:
+        got = run(torch_mod, qb, kb, vb, p, mode, "simt")
+        ref = attention_forward(qf, kf, vf, mode, p)
+        assert np.abs(got - ref).max() <= tol(mode, p)
+
+
+def test_nonzero_stream_and_preallocated_out(torch_mod):
+    torch = torch_mod
+    from lssar_attn_fwd_gb300 import api
+    qb, kb, vb = make_qkv(1, 2, 256, 64, seed=9)
+    q, k, v = (to_dev(torch, t) for t in (qb, kb, vb))
+    out = torch.full_like(q, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        api.lssar_attn_fwd(q, k, v, p=3, mode=MODE_LSSAR, out=out)
+    s.synchronize()
+    ref = attention_forward(*(bf16_bits_to_f64(t) for t in (qb, kb, vb)), MODE_LSSAR, 3)
+    assert np.abs(out.float().cpu().numpy() - ref).max() <= 2e-2
