@@ -1,0 +1,367 @@
+#!/usr/bin/env python3
+"""Benchmark of the causal LSSAR attention forward on GB300.
+
+One step = one call of the whole hot path (normalisation prologue + the
+tcgen05 attention kernel) on one batch of seeded synthetic input resident in
+HBM.  Default workload: B=1 H=12 L=8192 d=64, LSSAR p=15, causal (the 8K
+extrapolation shape).  L2 is flushed (256 MiB write) before every timed step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--mode lssar|lssa|softmax] [--p P]
+
+Prints one JSON line on rank 0.  `--impl reference` times the float64 CPU
+oracle instead, on bounded samples of the same workload.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from lssar_attn_fwd_gb300.inputs import (  # noqa: E402
+    MODE_LSSA, MODE_LSSAR, MODE_SOFTMAX, WORKLOADS, bf16_bits_to_f64, make_qkv)
+
+METRIC = "LSSAR causal fwd TFLOP/s (3 GEMMs) + % BF16 tensor peak, 1×GB300, L=1K–16K"
+MODE_NAMES = {"lssar": MODE_LSSAR, "lssa": MODE_LSSA, "softmax": MODE_SOFTMAX}
+FLUSH_BYTES = 256 << 20
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def gemm_count(mode):
+    return 3 if mode == MODE_LSSAR else 2
+
+
+def flops(B, H, L, d, mode):
+    """Algorithmic flops: 2 flops per multiply-add, causal half of each GEMM."""
+    return gemm_count(mode) * 2.0 * B * H * d * L * (L + 1) / 2.0
+
+
+def causal_flops_rows(rows, d, mode):
+    return gemm_count(mode) * 2.0 * d * float(np.sum(rows))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_traffic(workload, mode, p):
+    """dram read+write bytes per launch of the attention kernel from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        src = os.path.join(ROOT, "lssar_attn_fwd_gb300", "csrc", "tc_kernel.cuh")
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        key = f"{workload}:{mode}:{p}"
+        ent = rec.get(key)
+        if ent and ent.get("tc_kernel_sha") == h:
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, 50 ms apart."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._reader, daemon=True).start()
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [s for (t, s) in self.samples if t0 <= t <= t1 and len(s) >= 8]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in win for i in range(4) if s[4 + i].lower().startswith("active")})
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in win if num(s[0]) is not None]
+        mx = [num(s[1]) for s in win if num(s[1]) is not None]
+        pw = [num(s[2]) for s in win if num(s[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(win)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_sample_rate(q, k, v, mode, p, seconds, max_blocks=None, block=64):
+    """Times the oracle on row blocks taken from the end of successive heads
+    (the longest rows) until `seconds` elapse.  Returns (flop/s, rows, blocks)."""
+    from oracle import attention_forward
+    B, H, L, d = q.shape
+    done_flops = 0.0
+    t0 = time.perf_counter()
+    nblk = 0
+    nrows = 0
+    while True:
+        h = nblk % (B * H)
+        b, hh = divmod(h, H)
+        hi = L - (nblk // (B * H)) * block % L
+        lo = max(1, hi - block + 1)
+        rows = np.arange(lo, hi + 1)
+        qf, kf, vf = (bf16_bits_to_f64(t[b, hh, :hi]) for t in (q, k, v))
+        attention_forward(qf, kf, vf, mode, p, rows=rows)
+        done_flops += causal_flops_rows(rows, d, mode)
+        nrows += rows.size
+        nblk += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_blocks and nblk >= max_blocks):
+            return done_flops / el, nrows, nblk, el
+
+
+def run_reference(args, wl, mode, p):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    q, k, v = make_qkv(*wl.shape, seed=0, structure=wl.structure)
+    from oracle import attention_forward
+    B, H, L, d = wl.shape
+    rows_per_step = 32
+
+    def step(s):
+        b, hh = divmod(s % (B * H), H)
+        hi = L - ((s // (B * H)) * rows_per_step) % L
+        lo = max(1, hi - rows_per_step + 1)
+        rows = np.arange(lo, hi + 1)
+        qf, kf, vf = (bf16_bits_to_f64(t[b, hh, :hi]) for t in (q, k, v))
+        attention_forward(qf, kf, vf, mode, p, rows=rows)
+        return causal_flops_rows(rows, d, mode)
+
+    for s in range(args.warmup):
+        step(s)
+    t0 = time.perf_counter()
+    total = 0.0
+    for s in range(args.steps):
+        total += step(s)
+    el = time.perf_counter() - t0
+    val = total / el / 1e12
+    sample = (f"{args.steps} steps x {rows_per_step} query rows (the last rows of successive heads) "
+              f"of the {wl.name} workload, float64 NumPy oracle")
+    line = {
+        "metric": METRIC, "value": val, "unit": "TFLOP/s", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(wl, mode, p),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(wl, mode, p):
+    mname = {MODE_LSSAR: "lssar", MODE_LSSA: "lssa", MODE_SOFTMAX: "softmax"}[mode]
+    return {"workload": f"{wl.name}: B={wl.B} H={wl.H} L={wl.L} d={wl.d} {mname}"
+                        + (f" p={p}" if mode == MODE_LSSAR else "") + f" causal, {wl.structure} bf16 inputs",
+            "B": wl.B, "H": wl.H, "L": wl.L, "d": wl.d, "mode": mname, "p": p if mode == MODE_LSSAR else None,
+            "gemms_counted": gemm_count(mode),
+            "l2": "flushed before every timed step (256 MiB write); inputs 37.7 MiB < L2",
+            "operands": "fp16 normalised q,k and bf16 P,V on tcgen05, fp32 accumulate, bf16 out"}
+
+
+def run_ours(args, wl, mode, p):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        torch.cuda.set_device(local)
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    from lssar_attn_fwd_gb300 import api
+    from lssar_attn_fwd_gb300.build import build
+    if rank == 0:
+        build()
+    if ws > 1:
+        dist.barrier()
+    api.load_library()
+
+    qb, kb, vb = make_qkv(*wl.shape, seed=rank, structure=wl.structure)
+    to_t = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    q_h, k_h, v_h = (to_t(b).pin_memory() for b in (qb, kb, vb))
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    out = torch.empty_like(q)
+    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    F = flops(wl.B, wl.H, wl.L, wl.d, mode)
+    launches_per_step = 1 if mode == MODE_SOFTMAX else 2
+
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for trio in ev:
+        for e in trio:
+            e.record(stream)
+    for _ in range(W):
+        flush.zero_()
+        api.lssar_attn_fwd(q, k, v, p=p, mode=mode, out=out)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    w0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        api.lssar_attn_fwd_profiled(q, k, v, p, mode, out, stream, ev[i][0], ev[i][1], ev[i][2])
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    w1 = time.time()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    kern_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    tot = sum(step_ms)
+    kern_mean = sum(kern_ms) / K
+    if ws > 1:
+        t = torch.tensor([tot, kern_mean], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot, kern_mean = t.tolist()
+    assert api.device_error_word() == 0, "device error word set during the timed region"
+
+    # end to end through the public API: pinned host inputs -> device -> kernel -> host output
+    KE = max(3, min(K, 100))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for it in range(2):
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(KE if it else 2):
+            q.copy_(q_h, non_blocking=True)
+            k.copy_(k_h, non_blocking=True)
+            v.copy_(v_h, non_blocking=True)
+            api.lssar_attn_fwd(q, k, v, p=p, mode=mode, out=out)
+            out_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / KE
+    if ws > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = t.item()
+    if sampler:
+        time.sleep(0.2)
+        sampler.stop()
+
+    if rank == 0:
+        ms = tot / K
+        value = ws * F / (ms * 1e-3) / 1e12
+        peak, peak_kind = peaks()
+        achieved = F / (kern_mean * 1e-3) / 1e12
+        cpu = None
+        if ws == 1 and not args.no_cpu_baseline:
+            rate, nrows, nblk, el = oracle_sample_rate(qb, kb, vb, mode, p, seconds=args.cpu_seconds)
+            cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": f"{nrows} query rows ({nblk} blocks of 64, the last rows of successive heads) "
+                             f"of this workload, float64 NumPy oracle, {el:.1f} s; cores = host threads "
+                             "available to its BLAS"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K, "warmup": W,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": config_dict(wl, mode, p),
+            "pct_bf16_peak": 100.0 * value / ws / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                         "kernel": "lssar_tc_kernel", "kernel_ms": kern_mean,
+                         "traffic": kernel_traffic(wl.name, mode, p)},
+            "e2e": {"value": ws * F / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2},
+            "gpu_launches": K * launches_per_step,
+            "clocks": sampler.summary(w0, w1) if sampler else None,
+            "wall_s_timed": w1 - w0,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="extrap", choices=sorted(WORKLOADS))
+    ap.add_argument("--mode", default=None, choices=sorted(MODE_NAMES))
+    ap.add_argument("--p", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = WORKLOADS[args.workload]
+    mode, p = wl.runs[0]
+    if args.mode is not None:
+        mode = MODE_NAMES[args.mode]
+    if args.p is not None:
+        p = args.p
+    if args.impl == "reference":
+        run_reference(args, wl, mode, p)
+    else:
+        run_ours(args, wl, mode, p)
+
+
+if __name__ == "__main__":
+    main()

@@ -37,8 +37,9 @@
 extern "C" {
 #endif
 
-/* Same type as the CUDA runtime's cudaStream_t. */
+/* Same types as the CUDA runtime's cudaStream_t and cudaEvent_t. */
 typedef struct CUstream_st *cudaStream_t;
+typedef struct CUevent_st *cudaEvent_t;
 
 typedef enum {
     LSSAR_MODE_SOFTMAX = 0, /* Softmax(q.k^T/sqrt(d)) on raw q, k (Background)       */
@@ -79,6 +80,18 @@ int lssar_attn_fwd(const void *q, const void *k, const void *v, void *out,
  */
 int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out,
                         int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
+
+/*
+ * lssar_attn_fwd with timing hooks: records `ev_start` on `stream` before the
+ * first kernel of the call (the normalisation prologue, LSSA/LSSAR modes),
+ * `ev_main` just before the attention kernel and `ev_end` after it.  Any event
+ * may be NULL (not recorded).  Events are created and owned by the caller.
+ * Used by the benchmark to time the attention kernel alone; the computation
+ * is identical to lssar_attn_fwd.
+ */
+int lssar_attn_fwd_profiled(const void *q, const void *k, const void *v, void *out,
+                            int B, int H, int L, int d, int p, int mode, cudaStream_t stream,
+                            cudaEvent_t ev_start, cudaEvent_t ev_main, cudaEvent_t ev_end);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *lssar_status_string(int status);

@@ -17,6 +17,7 @@ _LIB = None
 _EXPORTS = (
     "lssar_attn_fwd",
     "lssar_attn_fwd_simt",
+    "lssar_attn_fwd_profiled",
     "lssar_status_string",
     "lssar_device_error_word",
     "lssar_abi_version",
@@ -49,6 +50,8 @@ def load_library():
         fn = getattr(lib, name)
         fn.argtypes = fwd_args
         fn.restype = ctypes.c_int
+    lib.lssar_attn_fwd_profiled.argtypes = fwd_args + [ctypes.c_void_p] * 3
+    lib.lssar_attn_fwd_profiled.restype = ctypes.c_int
     lib.lssar_status_string.argtypes = [ctypes.c_int]
     lib.lssar_status_string.restype = ctypes.c_char_p
     lib.lssar_device_error_word.argtypes = [ctypes.POINTER(ctypes.c_uint)]
@@ -116,6 +119,21 @@ def lssar_attn_fwd(q, k, v, p=3, mode=MODE_LSSAR, out=None, stream=None):
 def lssar_attn_fwd_simt(q, k, v, p=3, mode=MODE_LSSAR, out=None, stream=None):
     """Same operation on the plain CUDA-core kernel (cross-check only)."""
     return _forward("lssar_attn_fwd_simt", q, k, v, p, mode, out, stream)
+
+
+def lssar_attn_fwd_profiled(q, k, v, p, mode, out, stream, ev_start, ev_main, ev_end):
+    """The tensor-core forward recording caller-owned torch.cuda.Events around
+    the prologue and the attention kernel (each event must have been recorded
+    once before, so that its CUDA handle exists)."""
+    B, H, L, d = q.shape
+    status = load_library().lssar_attn_fwd_profiled(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+        ctypes.c_void_p(out.data_ptr()), B, H, L, d, int(p), int(mode),
+        ctypes.c_void_p(stream.cuda_stream),
+        ctypes.c_void_p(ev_start.cuda_event), ctypes.c_void_p(ev_main.cuda_event),
+        ctypes.c_void_p(ev_end.cuda_event))
+    _check(status)
+    return out
 
 
 def device_error_word():

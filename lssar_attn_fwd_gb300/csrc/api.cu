@@ -70,12 +70,8 @@ cudaError_t device_pool(cudaMemPool_t *out) {
     return cudaSuccess;
 }
 
-}  // namespace
-
-extern "C" {
-
-int lssar_attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
-                   int d, int p, int mode, cudaStream_t stream) {
+int run_tc(const void *q, const void *k, const void *v, void *out, int B, int H, int L, int d,
+           int p, int mode, cudaStream_t stream, const lssar::Events &ev) {
     lssar::Problem pr;
     const int st = validate(q, k, v, out, B, H, L, d, p, mode, &pr);
     if (st != LSSAR_OK) return st;
@@ -86,9 +82,28 @@ int lssar_attn_fwd(const void *q, const void *k, const void *v, void *out, int B
         if (device_pool(&pool) != cudaSuccess) return LSSAR_ERR_CUDA;
         if (cudaMallocFromPoolAsync(&ws, ws_bytes, pool, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
     }
-    const cudaError_t e = lssar::launch_tc(pr, ws, stream);
+    const cudaError_t e = lssar::launch_tc(pr, ws, stream, ev);
     if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
     return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lssar_attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+                   int d, int p, int mode, cudaStream_t stream) {
+    return run_tc(q, k, v, out, B, H, L, d, p, mode, stream, lssar::Events());
+}
+
+int lssar_attn_fwd_profiled(const void *q, const void *k, const void *v, void *out, int B, int H,
+                            int L, int d, int p, int mode, cudaStream_t stream,
+                            cudaEvent_t ev_start, cudaEvent_t ev_main, cudaEvent_t ev_end) {
+    lssar::Events ev;
+    ev.start = ev_start;
+    ev.main = ev_main;
+    ev.end = ev_end;
+    return run_tc(q, k, v, out, B, H, L, d, p, mode, stream, ev);
 }
 
 int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out, int B, int H,

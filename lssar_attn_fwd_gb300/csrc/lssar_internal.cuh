@@ -20,10 +20,17 @@ struct Problem {
 // Plain CUDA-core kernel (one warp per query row).  Returns a cudaError_t.
 cudaError_t launch_simt(const Problem &pr, cudaStream_t stream);
 
+// Optional events recorded around the kernels of one call (NULL = skipped).
+struct Events {
+    cudaEvent_t start = nullptr;  // before the normalisation prologue
+    cudaEvent_t main = nullptr;   // before the attention kernel
+    cudaEvent_t end = nullptr;    // after the attention kernel
+};
+
 // Tensor-core path (tcgen05 + TMEM + TMA).  `ws` is device scratch of at
 // least tc_workspace_bytes(pr) bytes, 256-byte aligned.
 size_t tc_workspace_bytes(const Problem &pr);
-cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream);
+cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Events &ev = Events());
 
 // Reads and clears the device error word of the current device.
 cudaError_t read_and_clear_error_word(unsigned int *word);

@@ -17,14 +17,16 @@ __device__ unsigned g_error_word;
 // q_i / max(|q_i|, 1e-12) and k_j / max(|k_j|, 1e-12) rounded to fp16 (Key
 // design 1 of the notes: rows are L2-normalised before the score product).
 // Each row is handled by D/8 consecutive threads, 8 elements each.
+// Thread 0 also zeroes the attention kernel's work counter.
 template <int D>
 __global__ void __launch_bounds__(256) normalize_rows_fp16(const __nv_bfloat16 *__restrict__ q,
                                                            const __nv_bfloat16 *__restrict__ k,
                                                            __half *__restrict__ qh,
                                                            __half *__restrict__ kh,
-                                                           long long rows) {
+                                                           long long rows, unsigned *counter) {
     constexpr int G = D / 8;
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (tid == 0) *counter = 0u;
     const long long r = tid / G;
     const int part = (int)(tid % G);
     const bool live = r < 2 * rows;
@@ -134,31 +136,44 @@ cudaError_t error_word_ptr(unsigned **out) {
 
 }  // namespace
 
+namespace {
+constexpr size_t kCounterBytes = 256;
+
+size_t qk_bytes(const Problem &pr) {
+    return ((size_t)pr.B * pr.H * pr.L * pr.d * 2 + 255) & ~(size_t)255;
+}
+}  // namespace
+
+// Layout: [work counter, 256 B][normalised q, fp16][normalised k, fp16]; the
+// softmax mode needs only the counter.
 size_t tc_workspace_bytes(const Problem &pr) {
-    if (pr.mode == kSoftmax) return 0;
-    // normalised q and k in fp16, 256-byte aligned halves
-    const size_t half = ((size_t)pr.B * pr.H * pr.L * pr.d * 2 + 255) & ~(size_t)255;
-    return 2 * half;
+    if (pr.mode == kSoftmax) return kCounterBytes;
+    return kCounterBytes + 2 * qk_bytes(pr);
 }
 
-cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream) {
+cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Events &ev) {
     const int BH = pr.B * pr.H;
     const long long rows = (long long)BH * pr.L;
     const void *qsrc = pr.q, *ksrc = pr.k;
     CUtensorMapDataType qk_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (pr.mode != kSoftmax) {
-        const size_t half = tc_workspace_bytes(pr) / 2;
-        __half *qh = static_cast<__half *>(ws);
-        __half *kh = reinterpret_cast<__half *>(static_cast<char *>(ws) + half);
+    if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return cudaGetLastError();
+    unsigned *counter = static_cast<unsigned *>(ws);
+    if (pr.mode == kSoftmax) {
+        cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned), stream);
+        if (e != cudaSuccess) return e;
+    } else {
+        const size_t half = qk_bytes(pr);
+        __half *qh = reinterpret_cast<__half *>(static_cast<char *>(ws) + kCounterBytes);
+        __half *kh = reinterpret_cast<__half *>(static_cast<char *>(ws) + kCounterBytes + half);
         const long long threads = 2 * rows * (pr.d / 8);
         const long long blocks = (threads + 255) / 256;
         if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
         const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
         const auto *k = static_cast<const __nv_bfloat16 *>(pr.k);
         if (pr.d == 64)
-            normalize_rows_fp16<64><<<(unsigned)blocks, 256, 0, stream>>>(q, k, qh, kh, rows);
+            normalize_rows_fp16<64><<<(unsigned)blocks, 256, 0, stream>>>(q, k, qh, kh, rows, counter);
         else
-            normalize_rows_fp16<128><<<(unsigned)blocks, 256, 0, stream>>>(q, k, qh, kh, rows);
+            normalize_rows_fp16<128><<<(unsigned)blocks, 256, 0, stream>>>(q, k, qh, kh, rows, counter);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         qsrc = qh;
@@ -179,14 +194,19 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream) {
     prm.ln_d = logf((float)pr.d);
     prm.p = pr.p;
     prm.out = static_cast<__nv_bfloat16 *>(pr.out);
+    prm.counter = counter;
     cudaError_t e = error_word_ptr(&prm.err);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int grid = prm.n_items < sms ? prm.n_items : sms;
-    return pr.d == 64 ? dispatch<64>(pr, mq, mk, mv, prm, grid, stream)
-                      : dispatch<128>(pr, mq, mk, mv, prm, grid, stream);
+    if (ev.main && (e = cudaEventRecord(ev.main, stream)) != cudaSuccess) return e;
+    e = pr.d == 64 ? dispatch<64>(pr, mq, mk, mv, prm, grid, stream)
+                   : dispatch<128>(pr, mq, mk, mv, prm, grid, stream);
+    if (e != cudaSuccess) return e;
+    if (ev.end) e = cudaEventRecord(ev.end, stream);
+    return e;
 }
 
 cudaError_t read_and_clear_error_word(unsigned int *word) {

@@ -30,7 +30,13 @@
 //               over its own S columns, and runs the epilogue.
 // A work item is a pair of consecutive 128-row Q tiles of one head (2m, 2m+1)
 // sharing every K/V tile load; the two warpgroups ping-pong so that the MMA
-// of one tile overlaps the elementwise work of the other.
+// of one tile overlaps the elementwise work of the other.  Items are numbered
+// longest first; each CTA starts with item blockIdx.x and then takes the next
+// unclaimed item from a global counter (longest-processing-time-first), the
+// producer warp publishing each item to the other roles through a small
+// shared-memory queue.
+// Causal masking: on the diagonal tile the scaled scores above the diagonal
+// are replaced by -inf, for which every weight below evaluates to exactly 0.
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 #pragma once
 
@@ -50,7 +56,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a stuck wait gives up after
 
 // Error codes written to the device error word (first failure wins).
 enum : unsigned { kErrQFull = 1, kErrQEmpty, kErrKvFull, kErrKvEmpty, kErrSFull, kErrSFree,
-                  kErrOFull, kErrOFree };
+                  kErrOFull, kErrOFree, kErrItem };
 
 // Shared-memory descriptor strides.  K-major tiles (Q, K): rows of 128 bytes,
 // 8-row groups 1024 bytes apart.  MN-major V tiles: 16 keys per MMA = 2048
@@ -69,7 +75,8 @@ struct Params {
     float ln_d;      // ln(d)
     int p;           // LSSAR exponent (used by the generic power path)
     __nv_bfloat16 *out;
-    unsigned *err;   // device error word
+    unsigned *err;       // device error word
+    unsigned *counter;   // work counter, zero at launch
 };
 
 template <int D>
@@ -83,10 +90,15 @@ struct Cfg {
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
 };
 
+constexpr int kItemQ = 4;                     // depth of the work-item queue
+constexpr uint32_t kItemConsumers = 1 + 2 * kBM;   // MMA thread + both warpgroups
+
 struct __align__(8) Barriers {
     uint64_t q_full, q_empty;
     uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
     uint64_t kv_full[8], kv_empty[8];
+    uint64_t item_full[kItemQ], item_empty[kItemQ];
+    int item_q[kItemQ];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -108,27 +120,41 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Barriers
     }
 }
 
-// softplus(x)/ln 2 for z = x log2 e: max(z, 0) + log2(1 + 2^-|z|).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// softplus(x)/ln 2 for z = x log2 e: max(z, 0) + log2(1 + 2^-|z|), two lanes.
+// sp2(-inf) = 0.
+__device__ __forceinline__ float2 sp2x2(float2 z) {
+    const float2 u = make_float2(ptx::ex2(-fabsf(z.x)), ptx::ex2(-fabsf(z.y)));
+    const float2 v = __fadd2_rn(u, make_float2(1.f, 1.f));
+    return __fadd2_rn(make_float2(fmaxf(z.x, 0.f), fmaxf(z.y, 0.f)),
+                      make_float2(ptx::lg2(v.x), ptx::lg2(v.y)));
+}
+
 __device__ __forceinline__ float sp2(float z) {
     return fmaxf(z, 0.f) + ptx::lg2(1.f + ptx::ex2(-fabsf(z)));
 }
 
 template <int PK>
-__device__ __forceinline__ float powk(float r, int p) {
+__device__ __forceinline__ float2 powk2(float2 r, int p) {
     if constexpr (PK == 1) {
         return r;
     } else if constexpr (PK == 2) {
-        return r * r;
+        return __fmul2_rn(r, r);
     } else if constexpr (PK == 3) {
-        return r * r * r;
+        return __fmul2_rn(__fmul2_rn(r, r), r);
     } else if constexpr (PK == 15) {
-        const float r2 = r * r, r3 = r2 * r, r6 = r3 * r3, r12 = r6 * r6;
-        return r12 * r3;
+        const float2 r2 = __fmul2_rn(r, r), r3 = __fmul2_rn(r2, r), r6 = __fmul2_rn(r3, r3);
+        return __fmul2_rn(__fmul2_rn(r6, r6), r3);
     } else {
-        float acc = 1.f;
+        float2 acc = make_float2(1.f, 1.f);
         while (p) {
-            if (p & 1) acc *= r;
-            r *= r;
+            if (p & 1) acc = __fmul2_rn(acc, r);
+            r = __fmul2_rn(r, r);
             p >>= 1;
         }
         return acc;
@@ -142,54 +168,55 @@ struct RowConst {
     float m;       // softmax: row maximum of z
 };
 
-template <int MODE, int PK>
-__device__ __forceinline__ float weight(float z, const RowConst &rc, int p) {
-    if constexpr (MODE == kSoftmax) {
-        return ptx::ex2(z - rc.m);
-    } else if constexpr (MODE == kLssa) {
-        return sp2(z);
-    } else {
-        return powk<PK>(fmaxf(fmaf(sp2(z), rc.kappa, rc.beta), 0.f), p);
-    }
-}
-
-// One 32-column chunk of pass-1 statistics.
-template <int MODE, bool MASK>
-__device__ __forceinline__ void stats_chunk(const uint32_t (&r)[32], int col0, int trow, float a,
-                                            float &s1, float &m) {
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float z = __uint_as_float(r[j]) * a;
-        const bool keep = !MASK || (col0 + j <= trow);
-        if (keep) {
-            m = fmaxf(m, z);
-            if constexpr (MODE == kLssar) {
-                if (j & 1) acc1 += sp2(z); else acc0 += sp2(z);
-            }
-        }
-    }
-    s1 += acc0 + acc1;
-}
-
-// One 32-column chunk of pass-2 weights, packed to 16 bf16x2 words.
-template <int MODE, int PK, bool MASK>
-__device__ __forceinline__ void weight_chunk(const uint32_t (&r)[32], int col0, int trow,
-                                             const RowConst &rc, int p, float &s2, uint32_t *pk) {
-    float acc0 = 0.f, acc1 = 0.f;
+// Scores of one 32-column chunk to z = a * s in place; on the diagonal tile
+// the columns above row t become -inf.
+template <bool DIAG>
+__device__ __forceinline__ void to_z(uint32_t (&r)[32], int col0, int t, float a) {
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
-        float w0 = weight<MODE, PK>(__uint_as_float(r[j]) * rc.a, rc, p);
-        float w1 = weight<MODE, PK>(__uint_as_float(r[j + 1]) * rc.a, rc, p);
-        if (MASK) {
-            if (col0 + j > trow) w0 = 0.f;
-            if (col0 + j + 1 > trow) w1 = 0.f;
+        float2 z = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                              make_float2(a, a));
+        if (DIAG) {
+            if (col0 + j > t) z.x = -INFINITY;
+            if (col0 + j + 1 > t) z.y = -INFINITY;
         }
-        acc0 += w0;
-        acc1 += w1;
-        pk[j / 2] = ptx::pack_bf16x2(w0, w1);
+        r[j] = __float_as_uint(z.x);
+        r[j + 1] = __float_as_uint(z.y);
     }
-    s2 += acc0 + acc1;
+}
+
+// Pass-1 statistics of one chunk of z: running max and (LSSAR) softplus sum.
+template <int MODE>
+__device__ __forceinline__ void stats_z(const uint32_t (&r)[32], float2 &acc, float &m) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float2 z = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+        m = max3(m, z.x, z.y);
+        if constexpr (MODE == kLssar) acc = __fadd2_rn(acc, sp2x2(z));
+    }
+}
+
+// Pass-2 weights of one chunk of z, summed into acc and packed to 16 bf16x2.
+template <int MODE, int PK>
+__device__ __forceinline__ void weights_z(const uint32_t (&r)[32], const RowConst &rc, int p,
+                                          float2 &acc, uint32_t *pk) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float2 z = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+        float2 w;
+        if constexpr (MODE == kSoftmax) {
+            const float2 e = __fadd2_rn(z, make_float2(-rc.m, -rc.m));
+            w = make_float2(ptx::ex2(e.x), ptx::ex2(e.y));
+        } else if constexpr (MODE == kLssa) {
+            w = sp2x2(z);
+        } else {
+            const float2 t = __ffma2_rn(sp2x2(z), make_float2(rc.kappa, rc.kappa),
+                                        make_float2(rc.beta, rc.beta));
+            w = powk2<PK>(make_float2(fmaxf(t.x, 0.f), fmaxf(t.y, 0.f)), p);
+        }
+        acc = __fadd2_rn(acc, w);
+        pk[j / 2] = ptx::pack_bf16x2(w.x, w.y);
+    }
 }
 
 template <int D, int MODE, int PK>
@@ -226,6 +253,10 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), 1);
         }
+        for (int s = 0; s < kItemQ; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&bars->item_full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->item_empty[s]), kItemConsumers);
+        }
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -244,6 +275,16 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         m = prm.n_pairs - 1 - item / BH;   // longest pairs first
         bh = item % BH;
     };
+    // Consumer side of the work-item queue: returns false on a timed-out wait.
+    auto next_item = [&](uint32_t &qi, int &item) -> bool {
+        const uint32_t s = qi % kItemQ, use = qi / kItemQ;
+        ++qi;
+        if (!wait_bar(ptx::smem_u32(&bars->item_full[s]), use & 1, bars, prm.err, kErrItem))
+            return false;
+        item = *(volatile int *)&bars->item_q[s];
+        ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[s]));
+        return true;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -251,7 +292,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::prefetch_tensormap(&tmQ);
             ptx::prefetch_tensormap(&tmK);
             ptx::prefetch_tensormap(&tmV);
-            uint32_t ring_idx = 0, q_cnt = 0;
+            uint32_t ring_idx = 0, q_cnt = 0, qi = 0;
             bool ok = true;
             auto push = [&](const CUtensorMap *map, int tile, int bh) -> bool {
                 const uint32_t s = ring_idx % NS, use = ring_idx / NS;
@@ -267,17 +308,27 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ++ring_idx;
                 return true;
             };
-            for (int item = blockIdx.x; ok && item < prm.n_items; item += gridDim.x) {
+            while (ok) {
+                // claim and publish the next work item
+                const uint32_t s = qi % kItemQ, use = qi / kItemQ;
+                const int item = qi == 0 ? (int)blockIdx.x
+                                         : (int)(gridDim.x + atomicAdd(prm.counter, 1u));
+                ++qi;
+                if (use > 0 && !wait_bar(ptx::smem_u32(&bars->item_empty[s]), (use - 1) & 1, bars,
+                                         prm.err, kErrItem))
+                    break;
+                *(volatile int *)&bars->item_q[s] = item;
+                ptx::mbar_arrive(ptx::smem_u32(&bars->item_full[s]));
+                if (item >= prm.n_items) break;
+
                 int bh, m;
                 decode(item, bh, m);
                 const int qa = 2 * m, qb = 2 * m + 1;
                 const bool vb = qb < prm.n_qtiles;
                 const int nk = vb ? qb + 1 : qa + 1;
                 if (q_cnt > 0 && !wait_bar(ptx::smem_u32(&bars->q_empty), (q_cnt - 1) & 1, bars,
-                                           prm.err, kErrQEmpty)) {
-                    ok = false;
+                                           prm.err, kErrQEmpty))
                     break;
-                }
                 const uint32_t qf = ptx::smem_u32(&bars->q_full);
                 ptx::mbar_arrive_expect_tx(qf, (vb ? 2 : 1) * TB);
 #pragma unroll
@@ -301,7 +352,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t ring_idx = 0, q_cnt = 0;
+            uint32_t ring_idx = 0, q_cnt = 0, qi = 0;
             uint32_t sf_phase[2] = {0, 0}, of_phase[2] = {0, 0};
             bool s_pending[2] = {false, false}, o_pending[2] = {false, false};
             bool ok = true;
@@ -343,17 +394,16 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                 ptx::smem_desc_sw128(vb + k * 2048, kVLbo, kVSbo), kIdescPV,
                                 (accumulate || k > 0) ? 1u : 0u);
             };
-            for (int item = blockIdx.x; ok && item < prm.n_items; item += gridDim.x) {
+            int item;
+            while (ok && (ok = next_item(qi, item)) && item < prm.n_items) {
                 int bh, m;
                 decode(item, bh, m);
                 const int qa = 2 * m, qb = 2 * m + 1;
                 const bool vb = qb < prm.n_qtiles;
                 const int n_w[2] = {qa + 1, vb ? qb + 1 : 0};
                 const int nk = vb ? qb + 1 : qa + 1;
-                if (!wait_bar(ptx::smem_u32(&bars->q_full), q_cnt & 1, bars, prm.err, kErrQFull)) {
-                    ok = false;
+                if (!(ok = wait_bar(ptx::smem_u32(&bars->q_full), q_cnt & 1, bars, prm.err, kErrQFull)))
                     break;
-                }
                 ++q_cnt;
                 ptx::tc_fence_after();
                 uint32_t slot;
@@ -417,14 +467,17 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t s_free = ptx::smem_u32(&bars->s_free[w]);
         const uint32_t o_full = ptx::smem_u32(&bars->o_full[w]);
         const uint32_t o_free = ptx::smem_u32(&bars->o_free[w]);
-        uint32_t sf_phase = 0, of_phase = 0;
+        uint32_t sf_phase = 0, of_phase = 0, qi = 0;
         const float log2e = 1.4426950408889634f;
         auto wait_warp = [&](uint32_t bar, uint32_t parity, unsigned code) -> bool {
             const bool mine = wait_bar(bar, parity, bars, prm.err, code);
             return __all_sync(0xffffffffu, mine);
         };
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < prm.n_items; item += gridDim.x) {
+        int item;
+        while (ok) {
+            ok = __all_sync(0xffffffffu, next_item(qi, item));
+            if (!ok || item >= prm.n_items) break;
             int bh, m;
             decode(item, bh, m);
             const int qt = 2 * m + w;
@@ -441,53 +494,60 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             rc.beta = 0.f;
             rc.m = 0.f;
             if constexpr (kTwoPass) {
-                float s1 = 0.f, mx = -INFINITY;
+                float2 acc[4];
+                float mx[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    acc[c] = make_float2(0.f, 0.f);
+                    mx[c] = -INFINITY;
+                }
                 for (int kt = 0; kt < n; ++kt) {
                     if (!(ok = wait_warp(s_full, sf_phase, kErrSFull))) break;
                     sf_phase ^= 1;
                     ptx::tc_fence_after();
-                    uint32_t r0[32], r1[32], r2[32], r3[32];
-                    ptx::tmem_ld32(s_col + 0, r0);
-                    ptx::tmem_ld32(s_col + 32, r1);
-                    ptx::tmem_ld32(s_col + 64, r2);
-                    ptx::tmem_ld32(s_col + 96, r3);
+                    uint32_t r[4][32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_col + 32 * c, r[c]);
                     ptx::tmem_ld_wait();
-                    ptx::reg_fence(r0);
-                    ptx::reg_fence(r1);
-                    ptx::reg_fence(r2);
-                    ptx::reg_fence(r3);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) ptx::reg_fence(r[c]);
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(s_free);   // S may be overwritten: values are in registers
                     if (kt == qt) {
-                        stats_chunk<MODE, true>(r0, 0, t, rc.a, s1, mx);
-                        stats_chunk<MODE, true>(r1, 32, t, rc.a, s1, mx);
-                        stats_chunk<MODE, true>(r2, 64, t, rc.a, s1, mx);
-                        stats_chunk<MODE, true>(r3, 96, t, rc.a, s1, mx);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) to_z<true>(r[c], 32 * c, t, rc.a);
                     } else {
-                        stats_chunk<MODE, false>(r0, 0, t, rc.a, s1, mx);
-                        stats_chunk<MODE, false>(r1, 32, t, rc.a, s1, mx);
-                        stats_chunk<MODE, false>(r2, 64, t, rc.a, s1, mx);
-                        stats_chunk<MODE, false>(r3, 96, t, rc.a, s1, mx);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) to_z<false>(r[c], 32 * c, t, rc.a);
                     }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) stats_z<MODE>(r[c], acc[c], mx[c]);
                 }
                 if (!ok) break;
+                const float mxr = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 if constexpr (MODE == kSoftmax) {
-                    rc.m = mx;
+                    rc.m = mxr;
                 } else {
+                    const float s1 = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                                     ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
                     const float o = (row + 1 <= 3) ? 0.f : 1.f;
                     const float theta = o * s1 / fi;
-                    const float den = sp2(mx) - theta;
+                    const float spm = sp2(mxr);
+                    const float den = spm - theta;
                     if (den > 0.f) {
                         rc.kappa = 1.f / den;
                         rc.beta = -theta * rc.kappa;
                     } else {
-                        rc.kappa = 0.f;   // all-zero re-weighted row: uniform weights
-                        rc.beta = 1.f;
+                        // All-zero re-weighted row: only an exactly uniform LSSA row
+                        // (all sp equal) gets here; (sp / sp_max)^p = 1 on every
+                        // unmasked column gives the uniform prefix mean.
+                        rc.kappa = 1.f / spm;
+                        rc.beta = 0.f;
                     }
                 }
             }
             // pass 2: weights into TMEM (over the S columns), running row sum
-            float s2 = 0.f;
+            float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             for (int kt = 0; kt < n; ++kt) {
                 if (!(ok = wait_warp(s_full, sf_phase, kErrSFull))) break;
                 sf_phase ^= 1;
@@ -501,12 +561,14 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     ptx::reg_fence(r0);
                     ptx::reg_fence(r1);
                     if (kt == qt) {
-                        weight_chunk<MODE, PK, true>(r0, h * 64, t, rc, prm.p, s2, pk);
-                        weight_chunk<MODE, PK, true>(r1, h * 64 + 32, t, rc, prm.p, s2, pk + 16);
+                        to_z<true>(r0, h * 64, t, rc.a);
+                        to_z<true>(r1, h * 64 + 32, t, rc.a);
                     } else {
-                        weight_chunk<MODE, PK, false>(r0, h * 64, t, rc, prm.p, s2, pk);
-                        weight_chunk<MODE, PK, false>(r1, h * 64 + 32, t, rc, prm.p, s2, pk + 16);
+                        to_z<false>(r0, h * 64, t, rc.a);
+                        to_z<false>(r1, h * 64 + 32, t, rc.a);
                     }
+                    weights_z<MODE, PK>(r0, rc, prm.p, acc2[0], pk);
+                    weights_z<MODE, PK>(r1, rc, prm.p, acc2[1], pk + 16);
                     ptx::tmem_st32(s_col + h * 32, pk);
                 }
                 ptx::tmem_st_wait();
@@ -514,6 +576,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ptx::mbar_arrive(s_free);   // P(kt) is in TMEM
             }
             if (!ok) break;
+            const float s2 = (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
             // epilogue
             if (!(ok = wait_warp(o_full, of_phase, kErrOFull))) break;
             of_phase ^= 1;
@@ -531,15 +594,12 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 uint4 *dst = reinterpret_cast<uint4 *>(prm.out + ((size_t)bh * prm.L + row) * D);
 #pragma unroll
                 for (int c = 0; c < D / 8; ++c) {
+                    const uint32_t *oc = &o[c / 4][(c % 4) * 8];
                     uint4 u;
-                    u.x = ptx::pack_bf16x2(__uint_as_float(o[c / 4][(c % 4) * 8 + 0]) * inv,
-                                           __uint_as_float(o[c / 4][(c % 4) * 8 + 1]) * inv);
-                    u.y = ptx::pack_bf16x2(__uint_as_float(o[c / 4][(c % 4) * 8 + 2]) * inv,
-                                           __uint_as_float(o[c / 4][(c % 4) * 8 + 3]) * inv);
-                    u.z = ptx::pack_bf16x2(__uint_as_float(o[c / 4][(c % 4) * 8 + 4]) * inv,
-                                           __uint_as_float(o[c / 4][(c % 4) * 8 + 5]) * inv);
-                    u.w = ptx::pack_bf16x2(__uint_as_float(o[c / 4][(c % 4) * 8 + 6]) * inv,
-                                           __uint_as_float(o[c / 4][(c % 4) * 8 + 7]) * inv);
+                    u.x = ptx::pack_bf16x2(__uint_as_float(oc[0]) * inv, __uint_as_float(oc[1]) * inv);
+                    u.y = ptx::pack_bf16x2(__uint_as_float(oc[2]) * inv, __uint_as_float(oc[3]) * inv);
+                    u.z = ptx::pack_bf16x2(__uint_as_float(oc[4]) * inv, __uint_as_float(oc[5]) * inv);
+                    u.w = ptx::pack_bf16x2(__uint_as_float(oc[6]) * inv, __uint_as_float(oc[7]) * inv);
                     dst[c] = u;
                 }
             }
