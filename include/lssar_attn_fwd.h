@@ -56,7 +56,9 @@ typedef enum {
     LSSAR_ERR_MODE = -5,    /* unknown mode                                           */
     LSSAR_ERR_ALIGN = -6,   /* a pointer is not 16-byte aligned                       */
     LSSAR_ERR_CUDA = -7,    /* a CUDA call failed (launch, pool allocation, ...)      */
-    LSSAR_ERR_ALIAS = -8    /* out overlaps q, k or v                                 */
+    LSSAR_ERR_ALIAS = -8,   /* out overlaps q, k or v                                 */
+    LSSAR_ERR_SCRATCH = -9  /* lssar_attn_fwd_noalloc: problem needs more scratch than
+                               LSSAR_NOALLOC_SCRATCH_BYTES                            */
 } lssar_status_t;
 
 /*
@@ -92,6 +94,42 @@ int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out,
 int lssar_attn_fwd_profiled(const void *q, const void *k, const void *v, void *out,
                             int B, int H, int L, int d, int p, int mode, cudaStream_t stream,
                             cudaEvent_t ev_start, cudaEvent_t ev_main, cudaEvent_t ev_end);
+
+/*
+ * Size of the fixed device scratch array used by lssar_attn_fwd_noalloc
+ * (32 MiB).  Every GPU on which the library is loaded holds it until the
+ * process exits.
+ */
+#define LSSAR_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * lssar_attn_fwd without any device memory allocation.
+ *
+ * The notes on the method have no counterpart of this: it exists for callers
+ * that cannot let a library allocate device memory while it runs -- for
+ * example inference-runtime plugins whose execute/enqueue step is not allowed
+ * to allocate, hosts that reserve their whole memory budget up front, and
+ * latency-critical loops where an allocation could block on the driver.
+ *
+ * Same operation, arguments and results as lssar_attn_fwd.  The caller still
+ * provides q, k, v and out; the temporary data (a work counter and the
+ * normalised q and k in fp16, 256 + 4*B*H*L*d bytes in LSSA/LSSAR mode, 256
+ * bytes in softmax mode) lives in one fixed device array of
+ * LSSAR_NOALLOC_SCRATCH_BYTES compiled into the library.  Problems that need
+ * more return LSSAR_ERR_SCRATCH before anything is launched (for example
+ * B*H*L*d must stay below about 8.4 million elements in LSSA/LSSAR mode).
+ * No cudaMalloc, cudaFree or pool allocation is made.
+ *
+ * The first call on a device looks up that device's copy of the array (and
+ * may make the CUDA driver load the library's device code); make that first
+ * call before any stream capture.  All calls share the one array per device
+ * and it keeps the previous call's contents; the parts that must start at zero
+ * are cleared by each call on its stream.  Calls whose execution overlaps on
+ * the GPU (different streams, or different host threads, without ordering
+ * between them) race on the array: order them.
+ */
+int lssar_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *out,
+                           int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *lssar_status_string(int status);

@@ -18,6 +18,7 @@ _EXPORTS = (
     "lssar_attn_fwd",
     "lssar_attn_fwd_simt",
     "lssar_attn_fwd_profiled",
+    "lssar_attn_fwd_noalloc",
     "lssar_status_string",
     "lssar_device_error_word",
     "lssar_abi_version",
@@ -46,7 +47,7 @@ def load_library():
             "(there is no fallback implementation)")
     lib = ctypes.CDLL(path)
     fwd_args = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
-    for name in ("lssar_attn_fwd", "lssar_attn_fwd_simt"):
+    for name in ("lssar_attn_fwd", "lssar_attn_fwd_simt", "lssar_attn_fwd_noalloc"):
         fn = getattr(lib, name)
         fn.argtypes = fwd_args
         fn.restype = ctypes.c_int

@@ -89,6 +89,11 @@ int run_tc(const void *q, const void *k, const void *v, void *out, int B, int H,
 
 }  // namespace
 
+int lssar::validate_args(const void *q, const void *k, const void *v, void *out, int B, int H,
+                         int L, int d, int p, int mode, lssar::Problem *pr) {
+    return validate(q, k, v, out, B, H, L, d, p, mode, pr);
+}
+
 extern "C" {
 
 int lssar_attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
@@ -125,6 +130,7 @@ const char *lssar_status_string(int status) {
         case LSSAR_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
         case LSSAR_ERR_CUDA: return "CUDA error";
         case LSSAR_ERR_ALIAS: return "out overlaps q, k or v";
+        case LSSAR_ERR_SCRATCH: return "problem needs more scratch than the fixed no-alloc array";
         default: return "unknown status";
     }
 }

@@ -17,6 +17,11 @@ struct Problem {
     int B, H, L, d, p, mode;
 };
 
+// Host-side argument checks of the C ABI (no CUDA call); LSSAR_OK or a
+// negative status.  Fills *pr on success.
+int validate_args(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
+                  int d, int p, int mode, Problem *pr);
+
 // Plain CUDA-core kernel (one warp per query row).  Returns a cudaError_t.
 cudaError_t launch_simt(const Problem &pr, cudaStream_t stream);
 
