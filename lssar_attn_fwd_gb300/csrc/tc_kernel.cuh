@@ -8,7 +8,8 @@
 //                      the L2-normalised rows (prepared in fp16 by a prologue)
 //   softmax scores     z_ij = log2(e) / sqrt(d) * q_i . k_j (raw bf16 rows)
 //   sp2(z) = max(z, 0) + log2(1 + 2^-|z|)  = softplus(x) / ln 2  for z = x log2 e
-//   pass 1 (LSSAR):    S1_i = sum_j sp2(z_ij),  m_i = max_j z_ij
+//   pass 1 (LSSAR):    S1_i = sum_j sp2(z_ij),  m_i = max_j z_ij, the softplus sum
+//                      taken as sum_j max(z,0) + log2 prod_j (1 + 2^-|z|)
 //   pass 1 (softmax):  m_i = max_j z_ij
 //   pass 2 weights:    LSSA     w = sp2(z)
 //                      LSSAR    w = max(sp2(z) kappa_i + beta_i, 0)^p with
@@ -185,14 +186,23 @@ __device__ __forceinline__ void to_z(uint32_t (&r)[32], int col0, int t, float a
     }
 }
 
-// Pass-1 statistics of one chunk of z: running max and (LSSAR) softplus sum.
+// Pass-1 statistics of one chunk of z: running max and, for LSSAR, the two
+// parts of sum_j sp2(z_j) = sum_j max(z_j, 0) + log2(prod_j (1 + 2^-|z_j|)).
+// The product form needs one FFMA per element instead of a log2: every factor
+// lies in (1, 2], so up to 64 factors multiply in fp32 without overflow (the
+// caller takes log2 of each 64-factor product once per tile).
 template <int MODE>
-__device__ __forceinline__ void stats_z(const uint32_t (&r)[32], float2 &acc, float &m) {
+__device__ __forceinline__ void stats_z(const uint32_t (&r)[32], float2 &relu_acc, float2 &prod,
+                                        float &m) {
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
         const float2 z = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
         m = max3(m, z.x, z.y);
-        if constexpr (MODE == kLssar) acc = __fadd2_rn(acc, sp2x2(z));
+        if constexpr (MODE == kLssar) {
+            const float2 u = make_float2(ptx::ex2(-fabsf(z.x)), ptx::ex2(-fabsf(z.y)));
+            prod = __ffma2_rn(prod, u, prod);
+            relu_acc = __fadd2_rn(relu_acc, make_float2(fmaxf(z.x, 0.f), fmaxf(z.y, 0.f)));
+        }
     }
 }
 
@@ -496,6 +506,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if constexpr (kTwoPass) {
                 float2 acc[4];
                 float mx[4];
+                float s1_log = 0.f;   // sum over tiles of log2 of the 64-factor products
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     acc[c] = make_float2(0.f, 0.f);
@@ -520,8 +531,17 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
                         for (int c = 0; c < 4; ++c) to_z<false>(r[c], 32 * c, t, rc.a);
                     }
+                    float2 prod[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) stats_z<MODE>(r[c], acc[c], mx[c]);
+                    for (int c = 0; c < 4; ++c) {
+                        prod[c] = make_float2(1.f, 1.f);
+                        stats_z<MODE>(r[c], acc[c], prod[c], mx[c]);
+                    }
+                    if constexpr (MODE == kLssar) {
+                        const float pa = (prod[0].x * prod[0].y) * (prod[1].x * prod[1].y);
+                        const float pb = (prod[2].x * prod[2].y) * (prod[3].x * prod[3].y);
+                        s1_log += ptx::lg2(pa) + ptx::lg2(pb);
+                    }
                 }
                 if (!ok) break;
                 const float mxr = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
@@ -529,7 +549,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     rc.m = mxr;
                 } else {
                     const float s1 = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-                                     ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+                                     ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y)) + s1_log;
                     const float o = (row + 1 <= 3) ? 0.f : 1.f;
                     const float theta = o * s1 / fi;
                     const float spm = sp2(mxr);
