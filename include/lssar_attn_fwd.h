@@ -50,7 +50,7 @@ typedef enum {
 typedef enum {
     LSSAR_OK = 0,
     LSSAR_ERR_NULL = -1,    /* a tensor pointer is NULL                               */
-    LSSAR_ERR_SHAPE = -2,   /* B, H or L < 1, or B*H*L*d beyond 2^40                  */
+    LSSAR_ERR_SHAPE = -2,   /* B, H or L < 1, L > 2^24, or B*H*L*d beyond 2^40         */
     LSSAR_ERR_HEADDIM = -3, /* d is not 64 or 128                                     */
     LSSAR_ERR_P = -4,       /* LSSAR mode with p < 1 or p > 1024                      */
     LSSAR_ERR_MODE = -5,    /* unknown mode                                           */

@@ -23,7 +23,7 @@ int validate(const void *q, const void *k, const void *v, void *out, int B, int 
     if (!q || !k || !v || !out) return LSSAR_ERR_NULL;
     if (mode != LSSAR_MODE_SOFTMAX && mode != LSSAR_MODE_LSSA && mode != LSSAR_MODE_LSSAR)
         return LSSAR_ERR_MODE;
-    if (B < 1 || H < 1 || L < 1) return LSSAR_ERR_SHAPE;
+    if (B < 1 || H < 1 || L < 1 || L > (1 << 24)) return LSSAR_ERR_SHAPE;
     if (d != 64 && d != 128) return LSSAR_ERR_HEADDIM;
     const unsigned long long elems = (unsigned long long)B * H * L * d;
     if (elems > (1ULL << 40)) return LSSAR_ERR_SHAPE;
@@ -123,7 +123,7 @@ const char *lssar_status_string(int status) {
     switch (status) {
         case LSSAR_OK: return "ok";
         case LSSAR_ERR_NULL: return "null tensor pointer";
-        case LSSAR_ERR_SHAPE: return "invalid shape (B, H, L >= 1 and B*H*L*d <= 2^40)";
+        case LSSAR_ERR_SHAPE: return "invalid shape (B, H >= 1, 1 <= L <= 2^24, B*H*L*d <= 2^40)";
         case LSSAR_ERR_HEADDIM: return "head dimension must be 64 or 128";
         case LSSAR_ERR_P: return "LSSAR exponent p must be in 1..1024";
         case LSSAR_ERR_MODE: return "unknown mode";

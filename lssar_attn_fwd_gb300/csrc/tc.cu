@@ -92,7 +92,17 @@ cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CU
                           const tc::Params &prm, int grid, cudaStream_t stream) {
     auto kern = tc::lssar_tc_kernel<D, MODE, PK>;
     constexpr int smem = tc::Cfg<D>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // The kernel moves registers from warpgroup 0 to the four score warpgroups
+    // (setmaxnreg); the re-allocation must fit in what the launch provides, or
+    // the increase would never be granted.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    const long long launch_regs = (long long)attr.numRegs * tc::kThreads;
+    const long long split_regs = 128LL * tc::kRegsCtl + 4LL * 128 * tc::kRegsScore;
+    if (tc::kRegSplit && (split_regs > launch_regs || attr.numRegs > tc::kRegsScore))
+        return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, tc::kThreads, smem, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError();

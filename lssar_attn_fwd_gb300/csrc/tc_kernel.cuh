@@ -7,7 +7,7 @@
 //   LSSA/LSSAR scores  z_ij = log2(e) * ln d * ln i * qh_i . kh_j, with qh, kh
 //                      the L2-normalised rows (prepared in fp16 by a prologue)
 //   softmax scores     z_ij = log2(e) / sqrt(d) * q_i . k_j (raw bf16 rows)
-//   sp2(z) = max(z, 0) + log2(1 + 2^-|z|)  = softplus(x) / ln 2  for z = x log2 e
+//   sp2(z) = log2(1 + 2^z) = softplus(x) / ln 2  for z = x log2 e
 //   pass 1 (LSSAR):    S1_i = sum_j sp2(z_ij),  m_i = max_j z_ij, the softplus sum
 //                      taken as sum_j max(z,0) + log2 prod_j (1 + 2^-|z|)
 //   pass 1 (softmax):  m_i = max_j z_ij
@@ -21,14 +21,27 @@
 //                      softmax  w = 2^(z - m_i)
 //   out_i = (sum_j w_ij v_j) / (sum_j w_ij)
 //
-// Structure (one persistent CTA per SM, 384 threads):
+// Structure (one persistent CTA per SM, 640 threads = 5 warpgroups):
 //   warp 0      TMA producer: Q tiles once per work item, then K (pass 1) and
 //               K, V (pass 2) tiles through an NS-stage shared-memory ring.
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer.
-//   warps 4-7   score warpgroup 0, warps 8-11 score warpgroup 1: thread t owns
-//               query row t of its Q tile (TMEM lane t), reads S from TMEM,
-//               computes statistics / weights, writes P (bf16) back into TMEM
-//               over its own S columns, and runs the epilogue.
+//   warps 2-3   idle (they complete warpgroup 0, which gives registers away)
+//   warps 4-19  four score warpgroups g = 0..3: Q tile w = g & 1 of the pair,
+//               column half h = g >> 1 of its 128-key S tile.  Thread t of a
+//               warpgroup owns query row t (TMEM lane t, lane quarter = warp % 4)
+//               and keys [64h, 64h+64) of every tile: it reads S from TMEM,
+//               computes statistics / weights, writes its 32 words of P (bf16
+//               pairs) back over the first half of its own S columns, and stores
+//               its half of the output row.  Each SM sub-partition therefore runs
+//               four math warps.  The two halves of a row combine their partial
+//               sums and maxima once per item through shared memory.
+// Registers: warpgroup 0 drops to kRegsCtl per thread, the score warpgroups
+// raise theirs to kRegsScore (setmaxnreg).
+// d = 64: P has TMEM columns of its own, so a warpgroup releases S as soon as
+// it has loaded it and the next S MMA overlaps the weight computation; P is
+// double-checked free by a commit after each P.V MMA.  d = 128: TMEM is full
+// with S and O, so P is written over the first half of each S column half and
+// S is released only once P is in place.
 // A work item is a pair of consecutive 128-row Q tiles of one head (2m, 2m+1)
 // sharing every K/V tile load; the two warpgroups ping-pong so that the MMA
 // of one tile overlaps the elementwise work of the other.  Items are numbered
@@ -38,7 +51,9 @@
 // shared-memory queue.
 // Causal masking: on the diagonal tile the scaled scores above the diagonal
 // are replaced by -inf, for which every weight below evaluates to exactly 0.
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// TMEM (512 columns): S0 [0,128), S1 [128,256); d = 64: P0 [256,320), P1 [320,384),
+// O0 [384,448), O1 [448,512); d = 128: O0 [256,384), O1 [384,512), and P_w over
+// S columns [128w, 128w+32) and [128w+64, 128w+96).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -52,12 +67,16 @@ namespace tc {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 384;
+constexpr bool kRegSplit = false;                  // setmaxnreg re-allocation
+constexpr int kThreads = kRegSplit ? 640 : 576;
+constexpr int kScoreWarp0 = kRegSplit ? 4 : 2;     // first score warp
+constexpr int kRegsCtl = 24;     // registers per thread of warpgroup 0 after the split
+constexpr int kRegsScore = 112;  // registers per thread of the score warpgroups
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a stuck wait gives up after 2 s
 
 // Error codes written to the device error word (first failure wins).
 enum : unsigned { kErrQFull = 1, kErrQEmpty, kErrKvFull, kErrKvEmpty, kErrSFull, kErrSFree,
-                  kErrOFull, kErrOFree, kErrItem };
+                  kErrOFull, kErrOFree, kErrItem, kErrPFull, kErrPFree };
 
 // Shared-memory descriptor strides.  K-major tiles (Q, K): rows of 128 bytes,
 // 8-row groups 1024 bytes apart.  MN-major V tiles: 16 keys per MMA = 2048
@@ -87,30 +106,43 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-    static constexpr int kBarBytes = 1024;
+    static constexpr int kBarBytes = 8192;
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
 };
 
 constexpr int kItemQ = 4;                     // depth of the work-item queue
-constexpr uint32_t kItemConsumers = 1 + 2 * kBM;   // MMA thread + both warpgroups
+constexpr uint32_t kItemConsumers = 1 + 4 * kBM;   // MMA thread + four warpgroups
+constexpr uint32_t kTileThreads = 2 * kBM;           // the two warpgroups of one Q tile
 
 struct __align__(8) Barriers {
     uint64_t q_full, q_empty;
-    uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
+    uint64_t s_full[2], s_free[2], o_full[2], o_free[2], p_full[2], p_free[2];
     uint64_t kv_full[8], kv_empty[8];
     uint64_t item_full[kItemQ], item_empty[kItemQ];
     int item_q[kItemQ];
     uint32_t tmem_base;
     int abort_flag;
+    // per-row partials exchanged by the two column halves: [tile][half][row]
+    float x_s1[2][2][kBM];
+    float x_m[2][2][kBM];
+    float x_s2[2][2][kBM];
 };
+
+static_assert(sizeof(Barriers) <= 8192, "barrier block too large");
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+constexpr uint32_t kSuspendNs = 1000000;   // hardware suspend per try_wait (upper bound)
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Barriers *b, unsigned *err,
                                          unsigned code) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((spin & 63u) == 0) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+        if ((spin & 15u) == 0) {
             if (*(volatile int *)&b->abort_flag) return false;
             if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
                 atomicCAS(err, 0u, code);
@@ -136,8 +168,18 @@ __device__ __forceinline__ float2 sp2x2(float2 z) {
                       make_float2(ptx::lg2(v.x), ptx::lg2(v.y)));
 }
 
+// sp2 evaluated directly as log2(1 + 2^z).  Exact in real arithmetic and free of
+// overflow here because |z| <= log2(e) ln(d) ln(L) * 1.001 < 117 for d <= 128 and
+// L <= 2^24 (the C ABI rejects longer sequences); for z < -24 the 1 + 2^z rounds
+// to 1 and the (tiny, < 1e-7) softplus reads 0.  sp2(-inf) = 0.
+__device__ __forceinline__ float2 sp2x2_direct(float2 z) {
+    const float2 e = make_float2(ptx::ex2(z.x), ptx::ex2(z.y));
+    const float2 v = __fadd2_rn(e, make_float2(1.f, 1.f));
+    return make_float2(ptx::lg2(v.x), ptx::lg2(v.y));
+}
+
 __device__ __forceinline__ float sp2(float z) {
-    return fmaxf(z, 0.f) + ptx::lg2(1.f + ptx::ex2(-fabsf(z)));
+    return ptx::lg2(1.f + ptx::ex2(z));
 }
 
 template <int PK>
@@ -218,9 +260,9 @@ __device__ __forceinline__ void weights_z(const uint32_t (&r)[32], const RowCons
             const float2 e = __fadd2_rn(z, make_float2(-rc.m, -rc.m));
             w = make_float2(ptx::ex2(e.x), ptx::ex2(e.y));
         } else if constexpr (MODE == kLssa) {
-            w = sp2x2(z);
+            w = sp2x2_direct(z);
         } else {
-            const float2 t = __ffma2_rn(sp2x2(z), make_float2(rc.kappa, rc.kappa),
+            const float2 t = __ffma2_rn(sp2x2_direct(z), make_float2(rc.kappa, rc.kappa),
                                         make_float2(rc.beta, rc.beta));
             w = powk2<PK>(make_float2(fmaxf(t.x, 0.f), fmaxf(t.y, 0.f)), p);
         }
@@ -245,6 +287,9 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     constexpr int NS = C::kStages;
     constexpr int TB = C::kTileBytes;
     constexpr bool kTwoPass = MODE != kLssa;
+    constexpr bool kSepP = D == 64;                       // P in TMEM columns of its own
+    constexpr int kPCol = 2 * kBN;                        // P_w at kPCol + 64 w (d = 64)
+    constexpr int kOCol = kSepP ? 2 * kBN + 128 : 2 * kBN;  // O_w at kOCol + D w
     // S = Q K^T: fp16 (normalised) operands for LSSA/LSSAR, raw bf16 for softmax.
     constexpr uint32_t kIdescS = ptx::idesc_f16(MODE == kSoftmax, kBM, kBN, false, false);
     // O += P V: P bf16 from TMEM (K-major), V bf16 MN-major.
@@ -255,9 +300,11 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ptx::mbar_init(ptx::smem_u32(&bars->q_empty), 1);
         for (int w = 0; w < 2; ++w) {
             ptx::mbar_init(ptx::smem_u32(&bars->s_full[w]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->s_free[w]), kBM);
+            ptx::mbar_init(ptx::smem_u32(&bars->s_free[w]), kTileThreads);
             ptx::mbar_init(ptx::smem_u32(&bars->o_full[w]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->o_free[w]), kBM);
+            ptx::mbar_init(ptx::smem_u32(&bars->o_free[w]), kTileThreads);
+            ptx::mbar_init(ptx::smem_u32(&bars->p_full[w]), kTileThreads);
+            ptx::mbar_init(ptx::smem_u32(&bars->p_free[w]), 1);
         }
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
@@ -279,6 +326,12 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    if constexpr (kRegSplit) {
+        if (warp < kScoreWarp0)
+            ptx::setmaxnreg_dec<kRegsCtl>();
+        else
+            ptx::setmaxnreg_inc<kRegsScore>();
+    }
 
     const int BH = prm.BH;
     auto decode = [&](int item, int &bh, int &m) {
@@ -363,7 +416,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t ring_idx = 0, q_cnt = 0, qi = 0;
-            uint32_t sf_phase[2] = {0, 0}, of_phase[2] = {0, 0};
+            uint32_t sf_phase[2] = {0, 0}, of_phase[2] = {0, 0}, pf_phase[2] = {0, 0};
             bool s_pending[2] = {false, false}, o_pending[2] = {false, false};
             bool ok = true;
             auto acquire = [&](uint32_t &slot) -> bool {
@@ -385,23 +438,32 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ptx::tc_fence_after();
                 return true;
             };
+            // Descriptors are built once; a K step moves the start address field
+            // (16-byte units, bits 0-13), which never carries for these offsets.
+            const uint64_t desc_q0 = ptx::smem_desc_sw128(ptx::smem_u32(sQ), kKmajorLbo, kKmajorSbo);
+            const uint64_t desc_k0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kKmajorLbo, kKmajorSbo);
+            const uint64_t desc_v0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kVLbo, kVSbo);
             auto issue_s = [&](int w, uint32_t kslot) {
-                const uint32_t qb = ptx::smem_u32(sQ + w * TB), kb = ptx::smem_u32(ring + kslot * TB);
+                const uint64_t dq = desc_q0 + (uint64_t)((w * TB) >> 4);
+                const uint64_t dk = desc_k0 + (uint64_t)((kslot * TB) >> 4);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-                    ptx::mma_ss(tmem + w * kBN, ptx::smem_desc_sw128(qb + off, kKmajorLbo, kKmajorSbo),
-                                ptx::smem_desc_sw128(kb + off, kKmajorLbo, kKmajorSbo), kIdescS, k > 0);
+                    const uint32_t off = ((k / 4) * 16384 + (k % 4) * 32) >> 4;
+                    ptx::mma_ss(tmem + w * kBN, dq + off, dk + off, kIdescS, k > 0);
                 }
                 ptx::mma_commit(ptx::smem_u32(&bars->s_full[w]));
                 s_pending[w] = true;
             };
             auto issue_pv = [&](int w, uint32_t vslot, bool accumulate) {
-                const uint32_t vb = ptx::smem_u32(ring + vslot * TB);
+                const uint64_t dv = desc_v0 + (uint64_t)((vslot * TB) >> 4);
+                // P words of keys 16k..16k+15: d = 64, 8k of P_w; d = 128, words
+                // (k%4)*8 of the S column half k/4
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k)
-                    ptx::mma_ts(tmem + 2 * kBN + w * D, tmem + w * kBN + k * 8,
-                                ptx::smem_desc_sw128(vb + k * 2048, kVLbo, kVSbo), kIdescPV,
+                    ptx::mma_ts(tmem + kOCol + w * D,
+                                kSepP ? tmem + kPCol + 64 * w + 8 * k
+                                      : tmem + w * kBN + (k / 4) * 64 + (k % 4) * 8,
+                                dv + (uint64_t)((k * 2048) >> 4), kIdescPV,
                                 (accumulate || k > 0) ? 1u : 0u);
             };
             int item;
@@ -435,48 +497,87 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         issue_s(w, slot);
                     }
                 ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[slot]));
+                auto wait_o_free = [&](int w) -> bool {
+                    if (!o_pending[w]) return true;
+                    if (!wait_bar(ptx::smem_u32(&bars->o_free[w]), of_phase[w], bars, prm.err,
+                                  kErrOFree))
+                        return false;
+                    of_phase[w] ^= 1;
+                    o_pending[w] = false;
+                    ptx::tc_fence_after();
+                    return true;
+                };
                 for (int kt = 0; ok && kt < nk; ++kt) {
                     const bool has_next = kt + 1 < nk;
                     uint32_t kslot = 0, vslot;
                     if (has_next && !(ok = acquire(kslot))) break;
-                    if (!(ok = acquire(vslot))) break;
-                    for (int w = 0; w < 2 && ok; ++w) {
-                        if (kt >= n_w[w]) continue;
-                        if (!(ok = touch_s(w))) break;   // P_w(kt) is in TMEM
-                        if (kt == 0 && o_pending[w]) {
-                            if (!(ok = wait_bar(ptx::smem_u32(&bars->o_free[w]), of_phase[w], bars,
-                                                prm.err, kErrOFree)))
+                    if constexpr (kSepP) {
+                        // next scores as soon as each warpgroup has loaded S(kt)
+                        for (int w = 0; w < 2 && ok; ++w)
+                            if (kt + 1 < n_w[w]) {
+                                if (!(ok = touch_s(w))) break;
+                                issue_s(w, kslot);
+                            }
+                        if (!ok) break;
+                        if (has_next) ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[kslot]));
+                        if (!(ok = acquire(vslot))) break;
+                        for (int w = 0; w < 2 && ok; ++w) {
+                            if (kt >= n_w[w]) continue;
+                            if (!(ok = wait_bar(ptx::smem_u32(&bars->p_full[w]), pf_phase[w], bars,
+                                                prm.err, kErrPFull)))
                                 break;
-                            of_phase[w] ^= 1;
-                            o_pending[w] = false;
+                            pf_phase[w] ^= 1;
                             ptx::tc_fence_after();
+                            if (kt == 0 && !(ok = wait_o_free(w))) break;
+                            issue_pv(w, vslot, kt > 0);
+                            ptx::mma_commit(ptx::smem_u32(&bars->p_free[w]));
+                            if (kt + 1 == n_w[w]) {
+                                ptx::mma_commit(ptx::smem_u32(&bars->o_full[w]));
+                                o_pending[w] = true;
+                            }
                         }
-                        issue_pv(w, vslot, kt > 0);
-                        if (kt + 1 < n_w[w]) {
-                            issue_s(w, kslot);
-                        } else {
-                            ptx::mma_commit(ptx::smem_u32(&bars->o_full[w]));
-                            o_pending[w] = true;
+                        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[vslot]));
+                    } else {
+                        if (!(ok = acquire(vslot))) break;
+                        for (int w = 0; w < 2 && ok; ++w) {
+                            if (kt >= n_w[w]) continue;
+                            if (!(ok = touch_s(w))) break;   // P_w(kt) is in TMEM
+                            if (kt == 0 && !(ok = wait_o_free(w))) break;
+                            issue_pv(w, vslot, kt > 0);
+                            if (kt + 1 < n_w[w]) {
+                                issue_s(w, kslot);
+                            } else {
+                                ptx::mma_commit(ptx::smem_u32(&bars->o_full[w]));
+                                o_pending[w] = true;
+                            }
                         }
+                        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[vslot]));
+                        if (has_next) ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[kslot]));
                     }
-                    ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[vslot]));
-                    if (has_next) ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[kslot]));
                 }
                 ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
             }
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else {
         // ------------------------------------------------------------ score warpgroups
-        const int w = (warp - 4) >> 2;              // warpgroup 0 or 1
-        const int t = threadIdx.x - 128 - 128 * w;  // row within the Q tile = TMEM lane
+        const int g = (warp - kScoreWarp0) >> 2;    // 0..3
+        const int w = g & 1;                        // Q tile of the pair
+        const int h = g >> 1;                       // column half of the S tile
+        const int t = (warp & 3) * 32 + lane;       // row within the Q tile = TMEM lane
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t s_col = tmem + lane_addr + w * kBN;
-        const uint32_t o_col = tmem + lane_addr + 2 * kBN + w * D;
+        const uint32_t s_col = tmem + lane_addr + w * kBN + h * 64;
+        const uint32_t o_col = tmem + lane_addr + kOCol + w * D + h * (D / 2);
+        const uint32_t p_col = kSepP ? tmem + lane_addr + kPCol + 64 * w + 32 * h : s_col;
+        const uint32_t p_full = ptx::smem_u32(&bars->p_full[w]);
+        const uint32_t p_free = ptx::smem_u32(&bars->p_free[w]);
+        uint32_t pf_phase = 0;
+        bool p_pending = false;   // a P.V MMA may still be reading this warpgroup's P words
         const uint32_t s_full = ptx::smem_u32(&bars->s_full[w]);
         const uint32_t s_free = ptx::smem_u32(&bars->s_free[w]);
         const uint32_t o_full = ptx::smem_u32(&bars->o_full[w]);
         const uint32_t o_free = ptx::smem_u32(&bars->o_free[w]);
+        const int pair_bar = 1 + w;                 // named barrier of this tile's two halves
         uint32_t sf_phase = 0, of_phase = 0, qi = 0;
         const float log2e = 1.4426950408889634f;
         auto wait_warp = [&](uint32_t bar, uint32_t parity, unsigned code) -> bool {
@@ -504,52 +605,45 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             rc.beta = 0.f;
             rc.m = 0.f;
             if constexpr (kTwoPass) {
-                float2 acc[4];
-                float mx[4];
+                float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                float mx[2] = {-INFINITY, -INFINITY};
                 float s1_log = 0.f;   // sum over tiles of log2 of the 64-factor products
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    acc[c] = make_float2(0.f, 0.f);
-                    mx[c] = -INFINITY;
-                }
                 for (int kt = 0; kt < n; ++kt) {
                     if (!(ok = wait_warp(s_full, sf_phase, kErrSFull))) break;
                     sf_phase ^= 1;
                     ptx::tc_fence_after();
-                    uint32_t r[4][32];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_col + 32 * c, r[c]);
+                    uint32_t r[2][32];
+                    ptx::tmem_ld32(s_col, r[0]);
+                    ptx::tmem_ld32(s_col + 32, r[1]);
                     ptx::tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) ptx::reg_fence(r[c]);
+                    ptx::reg_fence(r[0]);
+                    ptx::reg_fence(r[1]);
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(s_free);   // S may be overwritten: values are in registers
                     if (kt == qt) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) to_z<true>(r[c], 32 * c, t, rc.a);
+                        to_z<true>(r[0], 64 * h, t, rc.a);
+                        to_z<true>(r[1], 64 * h + 32, t, rc.a);
                     } else {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) to_z<false>(r[c], 32 * c, t, rc.a);
+                        to_z<false>(r[0], 64 * h, t, rc.a);
+                        to_z<false>(r[1], 64 * h + 32, t, rc.a);
                     }
-                    float2 prod[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        prod[c] = make_float2(1.f, 1.f);
-                        stats_z<MODE>(r[c], acc[c], prod[c], mx[c]);
-                    }
-                    if constexpr (MODE == kLssar) {
-                        const float pa = (prod[0].x * prod[0].y) * (prod[1].x * prod[1].y);
-                        const float pb = (prod[2].x * prod[2].y) * (prod[3].x * prod[3].y);
-                        s1_log += ptx::lg2(pa) + ptx::lg2(pb);
-                    }
+                    float2 prod[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
+                    stats_z<MODE>(r[0], acc[0], prod[0], mx[0]);
+                    stats_z<MODE>(r[1], acc[1], prod[1], mx[1]);
+                    if constexpr (MODE == kLssar)
+                        s1_log += ptx::lg2((prod[0].x * prod[0].y) * (prod[1].x * prod[1].y));
                 }
                 if (!ok) break;
-                const float mxr = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                // combine the two column halves of the row
+                bars->x_m[w][h][t] = fmaxf(mx[0], mx[1]);
+                if constexpr (MODE == kLssar)
+                    bars->x_s1[w][h][t] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + s1_log;
+                named_bar_sync(pair_bar, kTileThreads);
+                const float mxr = fmaxf(bars->x_m[w][0][t], bars->x_m[w][1][t]);
                 if constexpr (MODE == kSoftmax) {
                     rc.m = mxr;
                 } else {
-                    const float s1 = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-                                     ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y)) + s1_log;
+                    const float s1 = bars->x_s1[w][0][t] + bars->x_s1[w][1][t];
                     const float o = (row + 1 <= 3) ? 0.f : 1.f;
                     const float theta = o * s1 / fi;
                     const float spm = sp2(mxr);
@@ -566,54 +660,75 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                 }
             }
-            // pass 2: weights into TMEM (over the S columns), running row sum
+            // pass 2: weights into TMEM, running row sum
             float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             for (int kt = 0; kt < n; ++kt) {
                 if (!(ok = wait_warp(s_full, sf_phase, kErrSFull))) break;
                 sf_phase ^= 1;
                 ptx::tc_fence_after();
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t r0[32], r1[32], pk[32];
-                    ptx::tmem_ld32(s_col + h * 64, r0);
-                    ptx::tmem_ld32(s_col + h * 64 + 32, r1);
-                    ptx::tmem_ld_wait();
-                    ptx::reg_fence(r0);
-                    ptx::reg_fence(r1);
-                    if (kt == qt) {
-                        to_z<true>(r0, h * 64, t, rc.a);
-                        to_z<true>(r1, h * 64 + 32, t, rc.a);
-                    } else {
-                        to_z<false>(r0, h * 64, t, rc.a);
-                        to_z<false>(r1, h * 64 + 32, t, rc.a);
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld32(s_col, r0);
+                ptx::tmem_ld32(s_col + 32, r1);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(r0);
+                ptx::reg_fence(r1);
+                if constexpr (kSepP) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(s_free);   // the next S MMA may start now
+                    if (p_pending) {
+                        if (!(ok = wait_warp(p_free, pf_phase, kErrPFree))) break;
+                        pf_phase ^= 1;
+                        ptx::tc_fence_after();
                     }
+                }
+                // each 16-word half of this thread's P row is stored as soon as it
+                // is ready (d = 128: over S columns already loaded above)
+                {
+                    uint32_t pk[16];
+                    if (kt == qt) to_z<true>(r0, 64 * h, t, rc.a);
+                    else to_z<false>(r0, 64 * h, t, rc.a);
                     weights_z<MODE, PK>(r0, rc, prm.p, acc2[0], pk);
-                    weights_z<MODE, PK>(r1, rc, prm.p, acc2[1], pk + 16);
-                    ptx::tmem_st32(s_col + h * 32, pk);
+                    ptx::tmem_st16(p_col, pk);
+                }
+                {
+                    uint32_t pk[16];
+                    if (kt == qt) to_z<true>(r1, 64 * h + 32, t, rc.a);
+                    else to_z<false>(r1, 64 * h + 32, t, rc.a);
+                    weights_z<MODE, PK>(r1, rc, prm.p, acc2[1], pk);
+                    ptx::tmem_st16(p_col + 16, pk);
                 }
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(s_free);   // P(kt) is in TMEM
+                if constexpr (kSepP) {
+                    ptx::mbar_arrive(p_full);   // P(kt) is in TMEM
+                    p_pending = true;
+                } else {
+                    ptx::mbar_arrive(s_free);   // P(kt) is in TMEM over the S columns
+                }
             }
             if (!ok) break;
-            const float s2 = (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
-            // epilogue
+            bars->x_s2[w][h][t] = (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
+            named_bar_sync(pair_bar, kTileThreads);
+            const float s2 = bars->x_s2[w][0][t] + bars->x_s2[w][1][t];
+            // epilogue: this half's D/2 output columns
             if (!(ok = wait_warp(o_full, of_phase, kErrOFull))) break;
             of_phase ^= 1;
             ptx::tc_fence_after();
-            uint32_t o[D / 32][32];
+            constexpr int NC = D / 64;   // 32-column chunks per half
+            uint32_t o[NC][32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(o_col + c * 32, o[c]);
+            for (int c = 0; c < NC; ++c) ptx::tmem_ld32(o_col + c * 32, o[c]);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) ptx::reg_fence(o[c]);
+            for (int c = 0; c < NC; ++c) ptx::reg_fence(o[c]);
             ptx::tc_fence_before();
             ptx::mbar_arrive(o_free);
             if (row < prm.L) {
                 const float inv = 1.f / s2;
-                uint4 *dst = reinterpret_cast<uint4 *>(prm.out + ((size_t)bh * prm.L + row) * D);
+                uint4 *dst = reinterpret_cast<uint4 *>(prm.out + ((size_t)bh * prm.L + row) * D +
+                                                       h * (D / 2));
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
+                for (int c = 0; c < D / 16; ++c) {
                     const uint32_t *oc = &o[c / 4][(c % 4) * 8];
                     uint4 u;
                     u.x = ptx::pack_bf16x2(__uint_as_float(oc[0]) * inv, __uint_as_float(oc[1]) * inv);

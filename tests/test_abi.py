@@ -61,6 +61,7 @@ def test_invalid_arguments(lib, name):
     assert call(lib, name, B=0) == -2
     assert call(lib, name, H=-1) == -2
     assert call(lib, name, L=0) == -2
+    assert call(lib, name, L=(1 << 24) + 1) == -2
     assert call(lib, name, B=1 << 20, H=1 << 20, L=1 << 10, d=64) == -2
     assert call(lib, name, d=96) == -3
     assert call(lib, name, d=256) == -3
