@@ -99,7 +99,8 @@ cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CU
     cudaError_t e = cudaFuncGetAttributes(&attr, kern);
     if (e != cudaSuccess) return e;
     const long long launch_regs = (long long)attr.numRegs * tc::kThreads;
-    const long long split_regs = 128LL * tc::kRegsCtl + 4LL * 128 * tc::kRegsScore;
+    const long long split_regs =
+        32LL * tc::kScoreWarp0 * tc::kRegsCtl + 2LL * tc::kTileThreads * tc::kRegsScore;
     if (tc::kRegSplit && (split_regs > launch_regs || attr.numRegs > tc::kRegsScore))
         return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

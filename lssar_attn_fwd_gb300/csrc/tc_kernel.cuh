@@ -204,6 +204,13 @@ __device__ __forceinline__ float2 powk2(float2 r, int p) {
     }
 }
 
+// A re-weighted row counts as all-zero when sp2(m) - theta is within the
+// evaluation error of sp2 (relative ~1e-6 from the MUFU approximations, and
+// the two passes evaluate it by different formulas; absolute 1e-7 where
+// 1 + 2^z rounds to 1): the spread of such a row cannot be resolved in fp32.
+constexpr float kDegenerateRel = 1e-4f;
+constexpr float kDegenerateAbs = 1e-6f;
+
 struct RowConst {
     float a;       // score scale: z = a * s
     float kappa;   // LSSAR slope
@@ -648,13 +655,14 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     const float theta = o * s1 / fi;
                     const float spm = sp2(mxr);
                     const float den = spm - theta;
-                    if (den > 0.f) {
+                    if (den > kDegenerateRel * spm + kDegenerateAbs) {
                         rc.kappa = 1.f / den;
                         rc.beta = -theta * rc.kappa;
                     } else {
-                        // All-zero re-weighted row: only an exactly uniform LSSA row
-                        // (all sp equal) gets here; (sp / sp_max)^p = 1 on every
-                        // unmasked column gives the uniform prefix mean.
+                        // All-zero re-weighted row: an exactly uniform LSSA row (all sp
+                        // equal), or one whose spread is below the softplus evaluation
+                        // error; (sp / sp_max)^p ~= 1 on every unmasked column gives the
+                        // uniform prefix mean.
                         rc.kappa = 1.f / spm;
                         rc.beta = 0.f;
                     }
