@@ -134,6 +134,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(win)}
 
 
+def reduce_max_over_ranks(values, device):
+    """Element-wise max over all ranks of a list of floats (no-op on one rank).
+
+    Used for the step and kernel times: the job is as slow as its slowest rank.
+    """
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in values]
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tflops(world_size, flops_per_rank_step, ms_per_step):
+    """Units processed by all ranks divided by the (slowest rank's) step time."""
+    return world_size * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -272,12 +291,7 @@ def run_ours(args, wl, mode, p):
     w1 = time.time()
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
     kern_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    tot = sum(step_ms)
-    kern_mean = sum(kern_ms) / K
-    if ws > 1:
-        t = torch.tensor([tot, kern_mean], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot, kern_mean = t.tolist()
+    tot, kern_mean = reduce_max_over_ranks([sum(step_ms), sum(kern_ms) / K], dev)
     assert api.device_error_word() == 0, "device error word set during the timed region"
 
     # end to end through the public API: pinned host inputs -> device -> kernel -> host output
@@ -294,18 +308,14 @@ def run_ours(args, wl, mode, p):
             out_h.copy_(out, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / KE
-    if ws > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms = reduce_max_over_ranks([e0.elapsed_time(e1) / KE], dev)[0]
     if sampler:
         time.sleep(0.2)
         sampler.stop()
 
     if rank == 0:
         ms = tot / K
-        value = ws * F / (ms * 1e-3) / 1e12
+        value = whole_job_tflops(ws, F, ms)
         peak, peak_kind = peaks()
         achieved = F / (kern_mean * 1e-3) / 1e12
         cpu = None
@@ -324,7 +334,7 @@ def run_ours(args, wl, mode, p):
                          "frac": achieved / peak, "peak_source": f"{peak_kind} bf16_tflops (burst)",
                          "kernel": "lssar_tc_kernel", "kernel_ms": kern_mean,
                          "traffic": kernel_traffic(wl.name, mode, p)},
-            "e2e": {"value": ws * F / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": whole_job_tflops(ws, F, e2e_ms), "unit": "TFLOP/s",
                     "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2},
             "gpu_launches": K * launches_per_step,
