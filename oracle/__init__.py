@@ -14,7 +14,10 @@ from .lssar_oracle import (  # noqa: F401
     MODE_SOFTMAX,
     MODE_LSSA,
     MODE_LSSAR,
+    MODE_SOFTMAX_RW,
+    MODE_SIGMOID_RW,
     softplus,
+    sigmoid,
     l2_normalize_rows,
     length_scale,
     bias_o,

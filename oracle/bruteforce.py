@@ -14,6 +14,8 @@ import math
 MODE_SOFTMAX = 0
 MODE_LSSA = 1
 MODE_LSSAR = 2
+MODE_SOFTMAX_RW = 3
+MODE_SIGMOID_RW = 4
 
 
 def _dot(a, b):
@@ -27,12 +29,12 @@ def attention_bruteforce(q, k, v, mode, p=3, o_override=None):
     out = []
     for i in range(1, L + 1):
         qi = q[i - 1]
-        if mode == MODE_SOFTMAX:
+        if mode in (MODE_SOFTMAX, MODE_SOFTMAX_RW):
             sc = [_dot(qi, k[j]) / math.sqrt(d) for j in range(i)]
             top = max(sc)
             e = [math.exp(s - top) for s in sc]
             z = sum(e)
-            w = [x / z for x in e]
+            a = [x / z for x in e]
         else:
             nq = max(math.sqrt(_dot(qi, qi)), 1e-12)
             c = math.log(d) * math.log(i)
@@ -40,15 +42,18 @@ def attention_bruteforce(q, k, v, mode, p=3, o_override=None):
             for j in range(i):
                 nk = max(math.sqrt(_dot(k[j], k[j])), 1e-12)
                 cos = _dot(qi, k[j]) / (nq * nk)
-                a.append(math.log(1.0 + math.exp(c * cos)))
+                if mode == MODE_SIGMOID_RW:
+                    a.append(1.0 / (1.0 + math.exp(-c * cos)))
+                else:
+                    a.append(math.log(1.0 + math.exp(c * cos)))
             z = sum(a)
             a = [x / z for x in a]
-            if mode == MODE_LSSAR:
-                o = (0.0 if i <= 3 else 1.0) if o_override is None else float(o_override)
-                r = [max(i * x - o, 0.0) ** p for x in a]
-                t = sum(r)
-                w = [x / t for x in r] if t > 0.0 else [1.0 / i] * i
-            else:
-                w = a
+        if mode in (MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW):
+            o = (0.0 if i <= 3 else 1.0) if o_override is None else float(o_override)
+            r = [max(i * x - o, 0.0) ** p for x in a]
+            t = sum(r)
+            w = [x / t for x in r] if t > 0.0 else [1.0 / i] * i
+        else:
+            w = a
         out.append([sum(w[j] * v[j][t] for j in range(i)) for t in range(d)])
     return out

@@ -14,6 +14,10 @@ Models" (papernotes.org, arXiv 2501.13428):
 * Key design 3: the mask multiplies (0 replaces -inf) because Softplus is
   non-negative; it is applied after the Softplus.
 * The attention output is ``A V``.
+* Ablations (the notes' ablation table, 8K validation loss): re-weighting on
+  a softmax normaliser, ``A = Softmax(QK^T/sqrt(d) + M)`` followed by Key
+  design 2; and sigmoid + L1 + re-weighting, Key design 1 with Sigmoid in
+  place of Softplus, followed by Key design 2.
 
 Readings where the notes are silent (each is also listed in the design doc):
 natural log; 1-based row index i (= number of attended tokens); the L2 norm
@@ -39,6 +43,8 @@ import numpy as np
 MODE_SOFTMAX = 0
 MODE_LSSA = 1
 MODE_LSSAR = 2
+MODE_SOFTMAX_RW = 3     # ablation: re-weighting on a softmax normaliser
+MODE_SIGMOID_RW = 4     # ablation: sigmoid + L1 + re-weighting
 
 NORM_EPS = 1e-12
 
@@ -51,6 +57,14 @@ def softplus(x):
     """
     x = np.asarray(x, dtype=np.float64)
     return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def sigmoid(x):
+    """1 / (1 + e^-x), the nonnegative map of the sigmoid ablation, evaluated
+    without overflow for either sign of x."""
+    x = np.asarray(x, dtype=np.float64)
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
 
 
 def l2_normalize_rows(x, eps=NORM_EPS):
@@ -84,21 +98,23 @@ def _causal(rows, nk):
     return j <= np.asarray(rows, dtype=np.int64)[:, None]
 
 
-def lssa_rows(q_rows, k, rows, d):
+def lssa_rows(q_rows, k, rows, d, phi=None):
     """Rows of the LSSA matrix  [Key design 1].
 
     q_rows: raw queries of the requested rows, shape (n, d).
     k:      raw keys 1..max(rows), shape (>= max(rows), d).
     rows:   1-based row indices, shape (n,).
+    phi:    the nonnegative map, Softplus by default (Sigmoid for the ablation).
     Returns A of shape (n, max(rows)): zero where j > i, rows summing to 1.
     """
+    phi = softplus if phi is None else phi
     rows = np.asarray(rows, dtype=np.int64)
     nk = int(rows.max())
     qh = l2_normalize_rows(q_rows)
     kh = l2_normalize_rows(k[:nk])
     s = qh @ kh.T                                   # cosine scores, in [-1, 1]
     z = length_scale(rows, d)[:, None] * s          # (log d . log N) (.) QK^T
-    a = softplus(z) * _causal(rows, nk)             # Softplus first, then the 0/1 mask M'
+    a = phi(z) * _causal(rows, nk)                  # Softplus first, then the 0/1 mask M'
     return a / a.sum(axis=1, keepdims=True)         # L1 normalisation of each row
 
 
@@ -156,14 +172,16 @@ def attention_rows(q, k, v, rows, mode, p=3, o_override=None):
     rows = np.asarray(rows, dtype=np.int64)
     d = q.shape[-1]
     nk = int(rows.max())
-    if mode == MODE_SOFTMAX:
+    if mode in (MODE_SOFTMAX, MODE_SOFTMAX_RW):
         w = softmax_rows(q[rows - 1], k, rows, d)
     elif mode in (MODE_LSSA, MODE_LSSAR):
         w = lssa_rows(q[rows - 1], k, rows, d)
-        if mode == MODE_LSSAR:
-            w = reweight_rows(w, rows, p, o_override)
+    elif mode == MODE_SIGMOID_RW:
+        w = lssa_rows(q[rows - 1], k, rows, d, phi=sigmoid)
     else:
         raise ValueError(f"unknown mode {mode}")
+    if mode in (MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW):
+        w = reweight_rows(w, rows, p, o_override)
     return w @ v[:nk]
 
 

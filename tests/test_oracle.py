@@ -18,7 +18,9 @@ import pytest
 from oracle import (
     MODE_LSSA,
     MODE_LSSAR,
+    MODE_SIGMOID_RW,
     MODE_SOFTMAX,
+    MODE_SOFTMAX_RW,
     attention_bruteforce,
     attention_forward,
     lssa_rows,
@@ -27,7 +29,8 @@ from oracle import (
 )
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-ALL_MODES = (MODE_SOFTMAX, MODE_LSSA, MODE_LSSAR)
+ALL_MODES = (MODE_SOFTMAX, MODE_LSSA, MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW)
+RW_MODES = (MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW)
 
 
 def rand_qkv(L, d, seed, lead=()):
@@ -40,7 +43,8 @@ def rand_qkv(L, d, seed, lead=()):
 
 @pytest.mark.parametrize("L,d", [(1, 4), (5, 4), (17, 16), (32, 8)])
 @pytest.mark.parametrize("mode,p", [(MODE_SOFTMAX, 1), (MODE_LSSA, 1), (MODE_LSSAR, 1),
-                                    (MODE_LSSAR, 3), (MODE_LSSAR, 15)])
+                                    (MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_SOFTMAX_RW, 3),
+                                    (MODE_SOFTMAX_RW, 15), (MODE_SIGMOID_RW, 3), (MODE_SIGMOID_RW, 15)])
 def test_bruteforce_agrees(L, d, mode, p):
     q, k, v = rand_qkv(L, d, seed=L * 100 + d)
     ref = attention_bruteforce(q.tolist(), k.tolist(), v.tolist(), mode, p)
@@ -57,7 +61,8 @@ def test_bruteforce_agrees_zero_bias():
 
 # --- structural facts from the definitions --------------------------------
 
-@pytest.mark.parametrize("mode,p", [(MODE_SOFTMAX, 1), (MODE_LSSA, 1), (MODE_LSSAR, 3), (MODE_LSSAR, 15)])
+@pytest.mark.parametrize("mode,p", [(MODE_SOFTMAX, 1), (MODE_LSSA, 1), (MODE_LSSAR, 3), (MODE_LSSAR, 15),
+                                    (MODE_SOFTMAX_RW, 15), (MODE_SIGMOID_RW, 15)])
 def test_rows_sum_to_one(mode, p):
     # Every stage ends with an L1 normalisation (Key designs 1 and 2), so
     # V = ones gives an output of exactly ones.
@@ -66,7 +71,8 @@ def test_rows_sum_to_one(mode, p):
     np.testing.assert_allclose(out, 1.0, atol=1e-12)
 
 
-@pytest.mark.parametrize("mode,p", [(MODE_SOFTMAX, 1), (MODE_LSSA, 1), (MODE_LSSAR, 3), (MODE_LSSAR, 200)])
+@pytest.mark.parametrize("mode,p", [(MODE_SOFTMAX, 1), (MODE_LSSA, 1), (MODE_LSSAR, 3), (MODE_LSSAR, 200),
+                                    (MODE_SOFTMAX_RW, 15), (MODE_SIGMOID_RW, 3)])
 def test_first_row_is_first_value(mode, p):
     # Row 1 attends one token: log 1 = 0, softplus(0) = ln 2 normalises to 1.
     q, k, v = rand_qkv(10, 8, seed=4)
@@ -240,3 +246,94 @@ def test_length_scale_grows_sharpness():
     s32 = lssa_rows(q, k, np.array([32]), d)[0, :32].reshape(4, 8).sum(axis=0)
     ent = lambda w: -(w * np.log(w)).sum()
     assert ent(s32) < ent(s8)
+
+
+# --- ablation modes (the notes' ablation table) ---------------------------
+
+def test_softmax_reweight_p1_zero_bias_is_library_sdpa():
+    # p = 1 and O = 0 make re-weighting the identity, so re-weighting on a
+    # softmax normaliser reduces to plain softmax attention.
+    torch = pytest.importorskip("torch")
+    q, k, v = rand_qkv(40, 16, seed=21)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(k)[None], torch.from_numpy(v)[None],
+        is_causal=True).numpy()[0]
+    got = attention_forward(q, k, v, MODE_SOFTMAX_RW, 1, o_override=0.0)
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_softmax_reweight_rows_two_three_closed_form():
+    # Rows 2-3 (O = 0): weights proportional to softmax_j^p, i.e. to
+    # exp(p * q.k_j / sqrt(d)).
+    d = 8
+    q, k, v = rand_qkv(3, d, seed=22)
+    for p in (1, 3, 15):
+        out = attention_forward(q, k, v, MODE_SOFTMAX_RW, p)
+        for i in (2, 3):
+            sc = np.array([float(q[i - 1] @ k[j]) / math.sqrt(d) for j in range(i)])
+            w = np.exp(p * (sc - sc.max()))
+            np.testing.assert_allclose(out[i - 1], (w / w.sum()) @ v[:i], rtol=1e-10, atol=1e-12)
+
+
+def test_sigmoid_reweight_rows_two_three_closed_form():
+    # Rows 2-3 (O = 0): weights proportional to sigmoid(ln d ln i cos)^p.
+    for d in (4, 16):
+        q, k, v = rand_qkv(3, d, seed=30 + d)
+        for p in (1, 3, 15):
+            out = attention_forward(q, k, v, MODE_SIGMOID_RW, p)
+            for i in (2, 3):
+                c = math.log(d) * math.log(i)
+                sg = []
+                for j in range(i):
+                    cos = float(q[i - 1] @ k[j]) / (np.linalg.norm(q[i - 1]) * np.linalg.norm(k[j]))
+                    sg.append(1.0 / (1.0 + math.exp(-c * cos)))
+                w = np.array(sg) ** p
+                np.testing.assert_allclose(out[i - 1], (w / w.sum()) @ v[:i], rtol=1e-10, atol=1e-12)
+
+
+def test_sigmoid_golden_threshold_case():
+    # The hand-derived row-4 case holds for the sigmoid normaliser too:
+    # sigmoid(c) + sigmoid(-c) = 1 gives 4a - 1 = 2 sigmoid(+-c) - 1, positive
+    # for the two aligned keys only.
+    with open(os.path.join(GOLDEN, "threshold_row4.json")) as f:
+        g = json.load(f)
+    q, k, v = (np.array(g[n], dtype=np.float64) for n in ("q", "k", "v"))
+    for p in g["p_values"]:
+        out = attention_forward(q, k, v, MODE_SIGMOID_RW, p)
+        np.testing.assert_allclose(out[3], g["expected"]["lssar_row4_any_p"], atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", RW_MODES)
+def test_reweight_modes_identical_keys_prefix_mean(mode):
+    L, d = 30, 8
+    rng = np.random.default_rng(23)
+    q = rng.standard_normal((L, d))
+    k = np.tile(rng.standard_normal((1, d)), (L, 1))
+    v = rng.standard_normal((L, d))
+    mean = np.cumsum(v, axis=0) / np.arange(1, L + 1)[:, None]
+    np.testing.assert_allclose(attention_forward(q, k, v, mode, 15), mean, atol=1e-12)
+
+
+def test_reweight_modes_large_p_argmax():
+    # lim_{p->inf}: one-hot on the row's largest entry (Key design 2).  Rows
+    # are kept where the second-largest re-weighting input is below 0.9 of the
+    # largest, so that (0.9)^400 is negligible; the argmax is that of the raw
+    # scores (q.k for the softmax normaliser, the cosine for the sigmoid one).
+    L, d = 32, 16
+    rng = np.random.default_rng(24)
+    k = rng.standard_normal((L, d))
+    v = rng.standard_normal((L, d))
+    j = np.array([rng.integers(0, i + 1) for i in range(L)])
+    q = 4.0 * k[j] / np.linalg.norm(k[j], axis=1, keepdims=True)
+    kn = k / np.linalg.norm(k, axis=1, keepdims=True)
+    rows = np.arange(1, L + 1)
+    from oracle.lssar_oracle import softmax_rows, sigmoid
+    for mode, sc, a in ((MODE_SOFTMAX_RW, q @ k.T / math.sqrt(d), softmax_rows(q, k, rows, d)),
+                        (MODE_SIGMOID_RW, q @ kn.T, lssa_rows(q, k, rows, d, phi=sigmoid))):
+        sc = np.where(np.tril(np.ones((L, L), bool)), sc, -np.inf)
+        y = np.sort(np.maximum(rows[:, None] * a - 1.0, 0.0), axis=1)
+        clear = (y[:, -2] < 0.9 * y[:, -1]) & (rows >= 4)
+        assert clear.sum() > 10
+        out = attention_forward(q, k, v, mode, 400)
+        arg = np.argmax(sc, axis=1)
+        np.testing.assert_allclose(out[clear], v[arg[clear]], atol=1e-6)
