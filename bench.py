@@ -28,16 +28,22 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from lssar_attn_fwd_gb300.inputs import (  # noqa: E402
-    MODE_LSSA, MODE_LSSAR, MODE_SOFTMAX, WORKLOADS, bf16_bits_to_f64, make_qkv)
+    MODE_LSSA, MODE_LSSAR, MODE_SIGMOID_RW, MODE_SOFTMAX, MODE_SOFTMAX_RW, WORKLOADS,
+    bf16_bits_to_f64, make_qkv)
 
 METRIC = "LSSAR causal fwd TFLOP/s (3 GEMMs) + % BF16 tensor peak, 1×GB300, L=1K–16K"
-MODE_NAMES = {"lssar": MODE_LSSAR, "lssa": MODE_LSSA, "softmax": MODE_SOFTMAX}
+MODE_NAMES = {"lssar": MODE_LSSAR, "lssa": MODE_LSSA, "softmax": MODE_SOFTMAX,
+              "softmax_rw": MODE_SOFTMAX_RW, "sigmoid_rw": MODE_SIGMOID_RW}
+REWEIGHT_MODES = (MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW)
 FLUSH_BYTES = 256 << 20
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def gemm_count(mode):
-    return 3 if mode == MODE_LSSAR else 2
+    """GEMMs the method performs: re-weighting modes need the full first-stage
+    row sum before any weight, hence a second Q.K^T (3 GEMMs); LSSA and
+    softmax are counted with their 2 GEMMs."""
+    return 3 if mode in REWEIGHT_MODES else 2
 
 
 def flops(B, H, L, d, mode):
@@ -227,10 +233,10 @@ def run_reference(args, wl, mode, p):
 
 
 def config_dict(wl, mode, p):
-    mname = {MODE_LSSAR: "lssar", MODE_LSSA: "lssa", MODE_SOFTMAX: "softmax"}[mode]
+    mname = {v: k for k, v in MODE_NAMES.items()}[mode]
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} L={wl.L} d={wl.d} {mname}"
-                        + (f" p={p}" if mode == MODE_LSSAR else "") + f" causal, {wl.structure} bf16 inputs",
-            "B": wl.B, "H": wl.H, "L": wl.L, "d": wl.d, "mode": mname, "p": p if mode == MODE_LSSAR else None,
+                        + (f" p={p}" if mode in REWEIGHT_MODES else "") + f" causal, {wl.structure} bf16 inputs",
+            "B": wl.B, "H": wl.H, "L": wl.L, "d": wl.d, "mode": mname, "p": p if mode in REWEIGHT_MODES else None,
             "gemms_counted": gemm_count(mode),
             "l2": "flushed before every timed step (256 MiB write); inputs 37.7 MiB < L2",
             "operands": "fp16 normalised q,k and bf16 P,V on tcgen05, fp32 accumulate, bf16 out"}

@@ -13,6 +13,8 @@
  *       rows 1..3 and 1 otherwise, then each row is divided by its sum again.
  *   The output row i is sum_j A_ij v_j.
  *   Background (softmax mode): A = Softmax(q.k^T / sqrt(d) + causal -inf mask).
+ *   Ablation table (modes 3, 4): re-weighting applied to the softmax attention
+ *       above, and to LSSA with Sigmoid(x) = 1/(1+e^-x) in place of Softplus.
  *
  * A re-weighted row whose entries are all zero (possible only when the LSSA
  * row is exactly uniform) is 0/0 in the notes; this library returns the
@@ -42,9 +44,12 @@ typedef struct CUstream_st *cudaStream_t;
 typedef struct CUevent_st *cudaEvent_t;
 
 typedef enum {
-    LSSAR_MODE_SOFTMAX = 0, /* Softmax(q.k^T/sqrt(d)) on raw q, k (Background)       */
-    LSSAR_MODE_LSSA = 1,    /* Key design 1 only                                      */
-    LSSAR_MODE_LSSAR = 2    /* Key design 1 followed by Key design 2                  */
+    LSSAR_MODE_SOFTMAX = 0,    /* Softmax(q.k^T/sqrt(d)) on raw q, k (Background)    */
+    LSSAR_MODE_LSSA = 1,       /* Key design 1 only                                   */
+    LSSAR_MODE_LSSAR = 2,      /* Key design 1 followed by Key design 2               */
+    LSSAR_MODE_SOFTMAX_RW = 3, /* ablation: Softmax(q.k^T/sqrt(d)), then Key design 2 */
+    LSSAR_MODE_SIGMOID_RW = 4  /* ablation: Key design 1 with Sigmoid in place of
+                                  Softplus, then Key design 2                         */
 } lssar_mode_t;
 
 typedef enum {
@@ -52,7 +57,7 @@ typedef enum {
     LSSAR_ERR_NULL = -1,    /* a tensor pointer is NULL                               */
     LSSAR_ERR_SHAPE = -2,   /* B, H or L < 1, L > 2^24, or B*H*L*d beyond 2^40         */
     LSSAR_ERR_HEADDIM = -3, /* d is not 64 or 128                                     */
-    LSSAR_ERR_P = -4,       /* LSSAR mode with p < 1 or p > 1024                      */
+    LSSAR_ERR_P = -4,       /* re-weighting mode (2, 3, 4) with p < 1 or p > 1024     */
     LSSAR_ERR_MODE = -5,    /* unknown mode                                           */
     LSSAR_ERR_ALIGN = -6,   /* a pointer is not 16-byte aligned                       */
     LSSAR_ERR_CUDA = -7,    /* a CUDA call failed (launch, pool allocation, ...)      */
@@ -66,8 +71,8 @@ typedef enum {
  * kernel for sm_103a.
  *   q, k, v : [B, H, L, d] bfloat16, device, read only.
  *   out     : [B, H, L, d] bfloat16, device, written (row i of head (b, h)).
- *   p       : integer exponent of the re-weighting (LSSAR mode only, 1..1024;
- *             ignored in the other modes).
+ *   p       : integer exponent of the re-weighting (modes 2, 3, 4: 1..1024;
+ *             ignored in modes 0, 1).
  *   mode    : lssar_mode_t.
  * Returns LSSAR_OK or a negative lssar_status_t.
  */

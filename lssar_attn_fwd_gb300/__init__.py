@@ -4,7 +4,7 @@ The CUDA library is loaded lazily on the first call, so the input generator
 (`lssar_attn_fwd_gb300.inputs`) can be imported without a GPU or a build.
 """
 
-from .inputs import MODE_LSSA, MODE_LSSAR, MODE_SOFTMAX  # noqa: F401
+from .inputs import MODE_LSSA, MODE_LSSAR, MODE_SIGMOID_RW, MODE_SOFTMAX, MODE_SOFTMAX_RW  # noqa: F401
 
 
 def __getattr__(name):

@@ -10,7 +10,7 @@ built, or a call fails, an exception is raised.
 import ctypes
 import os
 
-from .inputs import MODE_LSSA, MODE_LSSAR, MODE_SOFTMAX  # noqa: F401
+from .inputs import MODE_LSSA, MODE_LSSAR, MODE_SIGMOID_RW, MODE_SOFTMAX, MODE_SOFTMAX_RW  # noqa: F401
 
 _LIB = None
 
@@ -111,7 +111,8 @@ def lssar_attn_fwd(q, k, v, p=3, mode=MODE_LSSAR, out=None, stream=None):
     """Causal LSSAR / LSSA / softmax attention forward on the tensor-core kernel.
 
     q, k, v: contiguous bf16 CUDA tensors [B, H, L, d] (d = 64 or 128).
-    p: re-weighting exponent (LSSAR mode).  mode: 0 softmax, 1 LSSA, 2 LSSAR.
+    p: re-weighting exponent (modes 2-4).  mode: 0 softmax, 1 LSSA, 2 LSSAR,
+    3 re-weighting on a softmax normaliser, 4 sigmoid + L1 + re-weighting.
     Runs asynchronously on ``stream`` (default: the current stream).
     """
     return _forward("lssar_attn_fwd", q, k, v, p, mode, out, stream)

@@ -21,20 +21,20 @@ bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
 int validate(const void *q, const void *k, const void *v, void *out, int B, int H, int L, int d,
              int p, int mode, lssar::Problem *pr) {
     if (!q || !k || !v || !out) return LSSAR_ERR_NULL;
-    if (mode != LSSAR_MODE_SOFTMAX && mode != LSSAR_MODE_LSSA && mode != LSSAR_MODE_LSSAR)
-        return LSSAR_ERR_MODE;
+    if (mode < LSSAR_MODE_SOFTMAX || mode > LSSAR_MODE_SIGMOID_RW) return LSSAR_ERR_MODE;
     if (B < 1 || H < 1 || L < 1 || L > (1 << 24)) return LSSAR_ERR_SHAPE;
     if (d != 64 && d != 128) return LSSAR_ERR_HEADDIM;
     const unsigned long long elems = (unsigned long long)B * H * L * d;
     if (elems > (1ULL << 40)) return LSSAR_ERR_SHAPE;
-    if (mode == LSSAR_MODE_LSSAR && (p < 1 || p > kMaxP)) return LSSAR_ERR_P;
+    const bool reweight = lssar::is_reweight(mode);
+    if (reweight && (p < 1 || p > kMaxP)) return LSSAR_ERR_P;
     for (const void *ptr : {q, k, v, static_cast<const void *>(out)})
         if (reinterpret_cast<uintptr_t>(ptr) & 15u) return LSSAR_ERR_ALIGN;
     const size_t bytes = (size_t)elems * 2;
     if (ranges_overlap(out, bytes, q, bytes) || ranges_overlap(out, bytes, k, bytes) ||
         ranges_overlap(out, bytes, v, bytes))
         return LSSAR_ERR_ALIAS;
-    *pr = lssar::Problem{q, k, v, out, B, H, L, d, mode == LSSAR_MODE_LSSAR ? p : 1, mode};
+    *pr = lssar::Problem{q, k, v, out, B, H, L, d, reweight ? p : 1, mode};
     return LSSAR_OK;
 }
 
@@ -125,7 +125,7 @@ const char *lssar_status_string(int status) {
         case LSSAR_ERR_NULL: return "null tensor pointer";
         case LSSAR_ERR_SHAPE: return "invalid shape (B, H >= 1, 1 <= L <= 2^24, B*H*L*d <= 2^40)";
         case LSSAR_ERR_HEADDIM: return "head dimension must be 64 or 128";
-        case LSSAR_ERR_P: return "LSSAR exponent p must be in 1..1024";
+        case LSSAR_ERR_P: return "re-weighting exponent p must be in 1..1024";
         case LSSAR_ERR_MODE: return "unknown mode";
         case LSSAR_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
         case LSSAR_ERR_CUDA: return "CUDA error";

@@ -6,7 +6,12 @@
 
 namespace lssar {
 
-enum Mode : int { kSoftmax = 0, kLssa = 1, kLssar = 2 };
+enum Mode : int { kSoftmax = 0, kLssa = 1, kLssar = 2, kSoftmaxRw = 3, kSigmoidRw = 4 };
+
+// Modes that end with the re-weighting step (and take the exponent p).
+__host__ __device__ constexpr bool is_reweight(int mode) { return mode == kLssar || mode == kSoftmaxRw || mode == kSigmoidRw; }
+// Modes whose scores use L2-normalised q, k (prepared by the prologue).
+__host__ __device__ constexpr bool uses_normalised_qk(int mode) { return mode == kLssa || mode == kLssar || mode == kSigmoidRw; }
 
 // Problem description after validation.  Tensors are [B, H, L, d] bf16.
 struct Problem {

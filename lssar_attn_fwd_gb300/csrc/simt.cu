@@ -17,6 +17,10 @@
 //              cancels in the final L1 normalisation); a row with
 //              softplus(m_i) <= theta_i is the all-zero 0/0 row: w = 1.
 //     softmax: w = exp(x - m_i)
+//   ablation modes, re-weighting of another normaliser phi (S1 = sum_j phi):
+//     softmax normaliser: phi = exp(x - m_i), x = q.k/sqrt(d)
+//     sigmoid normaliser: phi = 1/(1 + exp(-x)), x as in LSSA
+//     w = max((phi(x) - theta_i) / (phi(m_i) - theta_i), 0)^p
 #include <cuda_bf16.h>
 
 #include "lssar_internal.cuh"
@@ -40,6 +44,10 @@ __device__ __forceinline__ float warp_max(float x) {
 
 __device__ __forceinline__ float softplus_libm(float x) {
     return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+}
+
+__device__ __forceinline__ float sigmoid_libm(float x) {
+    return 1.f / (1.f + expf(-x));
 }
 
 __device__ __forceinline__ float powi(float x, int p) {
@@ -77,8 +85,8 @@ simt_fwd(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ 
     }
     qss = warp_sum(qss);
     __syncwarp();
-    const float qscale = (mode == kSoftmax)
-                             ? rsqrtf((float)D)
+    const bool raw = !uses_normalised_qk(mode);
+    const float qscale = raw ? rsqrtf((float)D)
                              : logf((float)D) * logf((float)i) / fmaxf(sqrtf(qss), 1e-12f);
 
     auto score = [&](int j) -> float {
@@ -97,27 +105,31 @@ simt_fwd(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ 
                 kss = fmaf(f.y, f.y, kss);
             }
         }
-        if (mode == kSoftmax) return dot * qscale;
+        if (raw) return dot * qscale;
         return dot * qscale / fmaxf(sqrtf(kss), 1e-12f);
     };
 
-    // Pass 1: row statistics.
+    // Pass 1: row statistics (max, then the sum of the normaliser's values).
     float s1 = 0.f, m = -INFINITY;
     if (mode != kLssa) {
-        for (int j = lane; j < i; j += 32) {
-            const float x = score(j);
-            m = fmaxf(m, x);
-            if (mode == kLssar) s1 += softplus_libm(x);
-        }
+        for (int j = lane; j < i; j += 32) m = fmaxf(m, score(j));
         m = warp_max(m);
+    }
+    auto phi = [&](float x) -> float {
+        if (mode == kSoftmaxRw) return expf(x - m);
+        if (mode == kSigmoidRw) return sigmoid_libm(x);
+        return softplus_libm(x);
+    };
+    if (is_reweight(mode)) {
+        for (int j = lane; j < i; j += 32) s1 += phi(score(j));
         s1 = warp_sum(s1);
     }
     float theta = 0.f, kappa = 0.f;
     bool degenerate = false;
-    if (mode == kLssar) {
+    if (is_reweight(mode)) {
         const float o = (i <= 3) ? 0.f : 1.f;
         theta = o * s1 / (float)i;
-        const float den = softplus_libm(m) - theta;
+        const float den = phi(m) - theta;
         degenerate = !(den > 0.f);
         kappa = degenerate ? 0.f : 1.f / den;
     }
@@ -137,7 +149,7 @@ simt_fwd(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ 
             } else if (mode == kLssa) {
                 w = softplus_libm(x);
             } else {
-                w = degenerate ? 1.f : powi(fmaxf((softplus_libm(x) - theta) * kappa, 0.f), p);
+                w = degenerate ? 1.f : powi(fmaxf((phi(x) - theta) * kappa, 0.f), p);
             }
         }
         s2 += w;

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "tc_kernel.cuh"
+#include "tc_dispatch.cuh"
 
 namespace lssar {
 
@@ -87,45 +88,6 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int BH, 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int MODE, int PK>
-cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                          const tc::Params &prm, int grid, cudaStream_t stream) {
-    auto kern = tc::lssar_tc_kernel<D, MODE, PK>;
-    constexpr int smem = tc::Cfg<D>::kSmemBytes;
-    // The kernel moves registers from warpgroup 0 to the four score warpgroups
-    // (setmaxnreg); the re-allocation must fit in what the launch provides, or
-    // the increase would never be granted.
-    cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
-    if (e != cudaSuccess) return e;
-    const long long launch_regs = (long long)attr.numRegs * tc::kThreads;
-    const long long split_regs =
-        32LL * tc::kScoreWarp0 * tc::kRegsCtl + 2LL * tc::kTileThreads * tc::kRegsScore;
-    if (tc::kRegSplit && (split_regs > launch_regs || attr.numRegs > tc::kRegsScore))
-        return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, tc::kThreads, smem, stream>>>(mq, mk, mv, prm);
-    return cudaGetLastError();
-}
-
-template <int D>
-cudaError_t dispatch(const Problem &pr, const CUtensorMap &mq, const CUtensorMap &mk,
-                     const CUtensorMap &mv, const tc::Params &prm, int grid, cudaStream_t s) {
-    switch (pr.mode) {
-        case kSoftmax: return launch_kernel<D, kSoftmax, 0>(mq, mk, mv, prm, grid, s);
-        case kLssa: return launch_kernel<D, kLssa, 0>(mq, mk, mv, prm, grid, s);
-        default:
-            switch (pr.p) {
-                case 1: return launch_kernel<D, kLssar, 1>(mq, mk, mv, prm, grid, s);
-                case 2: return launch_kernel<D, kLssar, 2>(mq, mk, mv, prm, grid, s);
-                case 3: return launch_kernel<D, kLssar, 3>(mq, mk, mv, prm, grid, s);
-                case 15: return launch_kernel<D, kLssar, 15>(mq, mk, mv, prm, grid, s);
-                default: return launch_kernel<D, kLssar, 0>(mq, mk, mv, prm, grid, s);
-            }
-    }
-}
-
 std::mutex g_sym_mutex;
 unsigned *g_err_ptr[64] = {};
 
@@ -158,7 +120,7 @@ size_t qk_bytes(const Problem &pr) {
 // Layout: [work counter, 256 B][normalised q, fp16][normalised k, fp16]; the
 // softmax mode needs only the counter.
 size_t tc_workspace_bytes(const Problem &pr) {
-    if (pr.mode == kSoftmax) return kCounterBytes;
+    if (!uses_normalised_qk(pr.mode)) return kCounterBytes;
     return kCounterBytes + 2 * qk_bytes(pr);
 }
 
@@ -169,7 +131,7 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
     CUtensorMapDataType qk_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (ev.start && cudaEventRecord(ev.start, stream) != cudaSuccess) return cudaGetLastError();
     unsigned *counter = static_cast<unsigned *>(ws);
-    if (pr.mode == kSoftmax) {
+    if (!uses_normalised_qk(pr.mode)) {
         cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned), stream);
         if (e != cudaSuccess) return e;
     } else {
@@ -213,8 +175,8 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int grid = prm.n_items < sms ? prm.n_items : sms;
     if (ev.main && (e = cudaEventRecord(ev.main, stream)) != cudaSuccess) return e;
-    e = pr.d == 64 ? dispatch<64>(pr, mq, mk, mv, prm, grid, stream)
-                   : dispatch<128>(pr, mq, mk, mv, prm, grid, stream);
+    e = pr.d == 64 ? tc::dispatch_d64(pr, mq, mk, mv, prm, grid, stream)
+                   : tc::dispatch_d128(pr, mq, mk, mv, prm, grid, stream);
     if (e != cudaSuccess) return e;
     if (ev.end) e = cudaEventRecord(ev.end, stream);
     return e;

@@ -1,0 +1,62 @@
+// Launch of the attention-kernel template instances, one translation unit
+// per head dimension (tc_d64.cu, tc_d128.cu) so that they compile in parallel.
+#pragma once
+
+#include "tc_kernel.cuh"
+
+namespace lssar {
+namespace tc {
+
+cudaError_t dispatch_d64(const Problem &pr, const CUtensorMap &mq, const CUtensorMap &mk,
+                         const CUtensorMap &mv, const Params &prm, int grid, cudaStream_t s);
+cudaError_t dispatch_d128(const Problem &pr, const CUtensorMap &mq, const CUtensorMap &mk,
+                          const CUtensorMap &mv, const Params &prm, int grid, cudaStream_t s);
+
+template <int D, int MODE, int PK>
+cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                          const Params &prm, int grid, cudaStream_t stream) {
+    auto kern = lssar_tc_kernel<D, MODE, PK>;
+    constexpr int smem = Cfg<D>::kSmemBytes;
+    // With the register split enabled, the re-allocation must fit in what the
+    // launch provides, or the increase would never be granted.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    const long long launch_regs = (long long)attr.numRegs * kThreads;
+    const long long split_regs = 32LL * kScoreWarp0 * kRegsCtl + 2LL * kTileThreads * kRegsScore;
+    if (kRegSplit && (split_regs > launch_regs || attr.numRegs > kRegsScore))
+        return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, prm);
+    return cudaGetLastError();
+}
+
+// Re-weighting modes: compile-time power chains for p in {1, 2, 3, 15},
+// square-and-multiply for any other p.
+template <int D, int MODE>
+cudaError_t dispatch_p(const Problem &pr, const CUtensorMap &mq, const CUtensorMap &mk,
+                       const CUtensorMap &mv, const Params &prm, int grid, cudaStream_t s) {
+    switch (pr.p) {
+        case 1: return launch_kernel<D, MODE, 1>(mq, mk, mv, prm, grid, s);
+        case 2: return launch_kernel<D, MODE, 2>(mq, mk, mv, prm, grid, s);
+        case 3: return launch_kernel<D, MODE, 3>(mq, mk, mv, prm, grid, s);
+        case 15: return launch_kernel<D, MODE, 15>(mq, mk, mv, prm, grid, s);
+        default: return launch_kernel<D, MODE, 0>(mq, mk, mv, prm, grid, s);
+    }
+}
+
+template <int D>
+cudaError_t dispatch(const Problem &pr, const CUtensorMap &mq, const CUtensorMap &mk,
+                     const CUtensorMap &mv, const Params &prm, int grid, cudaStream_t s) {
+    switch (pr.mode) {
+        case kSoftmax: return launch_kernel<D, kSoftmax, 0>(mq, mk, mv, prm, grid, s);
+        case kLssa: return launch_kernel<D, kLssa, 0>(mq, mk, mv, prm, grid, s);
+        case kLssar: return dispatch_p<D, kLssar>(pr, mq, mk, mv, prm, grid, s);
+        case kSoftmaxRw: return dispatch_p<D, kSoftmaxRw>(pr, mq, mk, mv, prm, grid, s);
+        default: return dispatch_p<D, kSigmoidRw>(pr, mq, mk, mv, prm, grid, s);
+    }
+}
+
+}  // namespace tc
+}  // namespace lssar

@@ -19,6 +19,15 @@
 //                               which the final L1 normalisation cancels; an all-zero
 //                               row (sp2(m_i) <= theta_i) gets w = 1 (prefix mean)
 //                      softmax  w = 2^(z - m_i)
+//   ablation modes (the notes' ablation table), both followed by re-weighting:
+//     softmax normaliser  z as in softmax; pass 1: m_i and S1_i = sum_j 2^(z-m_i)
+//                         (running max, sum rescaled per tile); a_ij = 2^(z-m)/S1,
+//                         w = max(2^(z-m) kappa_i + beta_i, 0)^p, theta_i = O_i S1_i / i,
+//                         kappa_i = 1/(1 - theta_i)
+//     sigmoid normaliser  z as in LSSA, sigma = 1/(1 + 2^-z); pass 1: m_i and
+//                         S1_i = sum_j sigma(z_ij); w = max(sigma kappa_i + beta_i, 0)^p,
+//                         kappa_i = 1/(sigma(m_i) - theta_i).  The registers hold -z
+//                         for this mode (scale -a, mask +inf) so 2^-z needs no negation.
 //   out_i = (sum_j w_ij v_j) / (sum_j w_ij)
 //
 // Structure (one persistent CTA per SM, 640 threads = 5 warpgroups):
@@ -153,6 +162,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Barriers
     }
 }
 
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -219,16 +234,18 @@ struct RowConst {
 };
 
 // Scores of one 32-column chunk to z = a * s in place; on the diagonal tile
-// the columns above row t become -inf.
-template <bool DIAG>
+// the columns above row t become -inf (+inf for the sigmoid mode, whose
+// registers hold -z).
+template <int MODE, bool DIAG>
 __device__ __forceinline__ void to_z(uint32_t (&r)[32], int col0, int t, float a) {
+    constexpr float kMasked = MODE == kSigmoidRw ? INFINITY : -INFINITY;
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
         float2 z = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
                               make_float2(a, a));
         if (DIAG) {
-            if (col0 + j > t) z.x = -INFINITY;
-            if (col0 + j + 1 > t) z.y = -INFINITY;
+            if (col0 + j > t) z.x = kMasked;
+            if (col0 + j + 1 > t) z.y = kMasked;
         }
         r[j] = __float_as_uint(z.x);
         r[j + 1] = __float_as_uint(z.y);
@@ -246,13 +263,48 @@ __device__ __forceinline__ void stats_z(const uint32_t (&r)[32], float2 &relu_ac
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
         const float2 z = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-        m = max3(m, z.x, z.y);
+        if constexpr (MODE == kSigmoidRw) {
+            // z holds -z here: m tracks min(-z); relu_acc sums sigmoid
+            m = min3(m, z.x, z.y);
+            const float2 v = __fadd2_rn(make_float2(ptx::ex2(z.x), ptx::ex2(z.y)), make_float2(1.f, 1.f));
+            relu_acc = __fadd2_rn(relu_acc, make_float2(ptx::rcp(v.x), ptx::rcp(v.y)));
+        } else {
+            m = max3(m, z.x, z.y);
+        }
         if constexpr (MODE == kLssar) {
             const float2 u = make_float2(ptx::ex2(-fabsf(z.x)), ptx::ex2(-fabsf(z.y)));
             prod = __ffma2_rn(prod, u, prod);
             relu_acc = __fadd2_rn(relu_acc, make_float2(fmaxf(z.x, 0.f), fmaxf(z.y, 0.f)));
         }
     }
+}
+
+// Softmax-normaliser statistics of one tile (two chunks of z): running max
+// m_run and sum s1 = sum_j 2^(z_j - m_run), rescaled when the max grows.
+// Fully masked prefixes (all -inf so far) leave both untouched.
+__device__ __forceinline__ void softmax_tile_stats(const uint32_t (&r0)[32], const uint32_t (&r1)[32],
+                                                   float &m_run, float &s1) {
+    float tm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        tm = max3(tm, __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]));
+        tm = max3(tm, __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]));
+    }
+    const float mn = fmaxf(m_run, tm);
+    if (mn == -INFINITY) return;
+    if (mn != m_run) s1 *= ptx::ex2(m_run - mn);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float2 e0 = __fadd2_rn(make_float2(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])),
+                                     make_float2(-mn, -mn));
+        const float2 e1 = __fadd2_rn(make_float2(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])),
+                                     make_float2(-mn, -mn));
+        acc0 = __fadd2_rn(acc0, make_float2(ptx::ex2(e0.x), ptx::ex2(e0.y)));
+        acc1 = __fadd2_rn(acc1, make_float2(ptx::ex2(e1.x), ptx::ex2(e1.y)));
+    }
+    s1 += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+    m_run = mn;
 }
 
 // Pass-2 weights of one chunk of z, summed into acc and packed to 16 bf16x2.
@@ -269,7 +321,17 @@ __device__ __forceinline__ void weights_z(const uint32_t (&r)[32], const RowCons
         } else if constexpr (MODE == kLssa) {
             w = sp2x2_direct(z);
         } else {
-            const float2 t = __ffma2_rn(sp2x2_direct(z), make_float2(rc.kappa, rc.kappa),
+            float2 phi;   // the normaliser's nonnegative value (up to a per-row factor)
+            if constexpr (MODE == kLssar) {
+                phi = sp2x2_direct(z);
+            } else if constexpr (MODE == kSoftmaxRw) {
+                const float2 e = __fadd2_rn(z, make_float2(-rc.m, -rc.m));
+                phi = make_float2(ptx::ex2(e.x), ptx::ex2(e.y));
+            } else {   // kSigmoidRw, z holds -z
+                const float2 v = __fadd2_rn(make_float2(ptx::ex2(z.x), ptx::ex2(z.y)), make_float2(1.f, 1.f));
+                phi = make_float2(ptx::rcp(v.x), ptx::rcp(v.y));
+            }
+            const float2 t = __ffma2_rn(phi, make_float2(rc.kappa, rc.kappa),
                                         make_float2(rc.beta, rc.beta));
             w = powk2<PK>(make_float2(fmaxf(t.x, 0.f), fmaxf(t.y, 0.f)), p);
         }
@@ -297,8 +359,9 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     constexpr bool kSepP = D == 64;                       // P in TMEM columns of its own
     constexpr int kPCol = 2 * kBN;                        // P_w at kPCol + 64 w (d = 64)
     constexpr int kOCol = kSepP ? 2 * kBN + 128 : 2 * kBN;  // O_w at kOCol + D w
-    // S = Q K^T: fp16 (normalised) operands for LSSA/LSSAR, raw bf16 for softmax.
-    constexpr uint32_t kIdescS = ptx::idesc_f16(MODE == kSoftmax, kBM, kBN, false, false);
+    // S = Q K^T: fp16 normalised operands (LSSA, LSSAR, sigmoid), raw bf16 (softmax modes).
+    constexpr bool kRawQK = !uses_normalised_qk(MODE);
+    constexpr uint32_t kIdescS = ptx::idesc_f16(kRawQK, kBM, kBN, false, false);
     // O += P V: P bf16 from TMEM (K-major), V bf16 MN-major.
     constexpr uint32_t kIdescPV = ptx::idesc_f16(true, kBM, D, false, true);
 
@@ -604,8 +667,10 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int row = qt * kBM + t;
             const float fi = (float)(row + 1);
             RowConst rc;
-            if constexpr (MODE == kSoftmax)
+            if constexpr (kRawQK)
                 rc.a = log2e * rsqrtf((float)D);
+            else if constexpr (MODE == kSigmoidRw)
+                rc.a = -log2e * prm.ln_d * logf(fi);   // registers hold -z
             else
                 rc.a = log2e * prm.ln_d * logf(fi);
             rc.kappa = 0.f;
@@ -613,8 +678,10 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             rc.m = 0.f;
             if constexpr (kTwoPass) {
                 float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                float mx[2] = {-INFINITY, -INFINITY};
+                constexpr float kInit = MODE == kSigmoidRw ? INFINITY : -INFINITY;
+                float mx[2] = {kInit, kInit};
                 float s1_log = 0.f;   // sum over tiles of log2 of the 64-factor products
+                float sm_run = -INFINITY, sm_sum = 0.f;   // softmax normaliser statistics
                 for (int kt = 0; kt < n; ++kt) {
                     if (!(ok = wait_warp(s_full, sf_phase, kErrSFull))) break;
                     sf_phase ^= 1;
@@ -628,27 +695,68 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(s_free);   // S may be overwritten: values are in registers
                     if (kt == qt) {
-                        to_z<true>(r[0], 64 * h, t, rc.a);
-                        to_z<true>(r[1], 64 * h + 32, t, rc.a);
+                        to_z<MODE, true>(r[0], 64 * h, t, rc.a);
+                        to_z<MODE, true>(r[1], 64 * h + 32, t, rc.a);
                     } else {
-                        to_z<false>(r[0], 64 * h, t, rc.a);
-                        to_z<false>(r[1], 64 * h + 32, t, rc.a);
+                        to_z<MODE, false>(r[0], 64 * h, t, rc.a);
+                        to_z<MODE, false>(r[1], 64 * h + 32, t, rc.a);
                     }
-                    float2 prod[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
-                    stats_z<MODE>(r[0], acc[0], prod[0], mx[0]);
-                    stats_z<MODE>(r[1], acc[1], prod[1], mx[1]);
-                    if constexpr (MODE == kLssar)
-                        s1_log += ptx::lg2((prod[0].x * prod[0].y) * (prod[1].x * prod[1].y));
+                    if constexpr (MODE == kSoftmaxRw) {
+                        softmax_tile_stats(r[0], r[1], sm_run, sm_sum);
+                    } else {
+                        float2 prod[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
+                        stats_z<MODE>(r[0], acc[0], prod[0], mx[0]);
+                        stats_z<MODE>(r[1], acc[1], prod[1], mx[1]);
+                        if constexpr (MODE == kLssar)
+                            s1_log += ptx::lg2((prod[0].x * prod[0].y) * (prod[1].x * prod[1].y));
+                    }
                 }
                 if (!ok) break;
-                // combine the two column halves of the row
-                bars->x_m[w][h][t] = fmaxf(mx[0], mx[1]);
-                if constexpr (MODE == kLssar)
-                    bars->x_s1[w][h][t] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + s1_log;
+                // combine the two column halves of the row (max of z, sum of phi)
+                if constexpr (MODE == kSoftmaxRw) {
+                    bars->x_m[w][h][t] = sm_run;
+                    bars->x_s1[w][h][t] = sm_sum;
+                } else if constexpr (MODE == kSigmoidRw) {
+                    bars->x_m[w][h][t] = -fminf(mx[0], mx[1]);
+                    bars->x_s1[w][h][t] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+                } else {
+                    bars->x_m[w][h][t] = fmaxf(mx[0], mx[1]);
+                    if constexpr (MODE == kLssar)
+                        bars->x_s1[w][h][t] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + s1_log;
+                }
                 named_bar_sync(pair_bar, kTileThreads);
-                const float mxr = fmaxf(bars->x_m[w][0][t], bars->x_m[w][1][t]);
+                const float m0 = bars->x_m[w][0][t], m1 = bars->x_m[w][1][t];
+                const float mxr = fmaxf(m0, m1);
                 if constexpr (MODE == kSoftmax) {
                     rc.m = mxr;
+                } else if constexpr (MODE == kSoftmaxRw) {
+                    // halves with no unmasked column carry m = -inf and a zero sum
+                    const float s1 = bars->x_s1[w][0][t] * ptx::ex2(m0 - mxr) +
+                                     bars->x_s1[w][1][t] * ptx::ex2(m1 - mxr);
+                    rc.m = mxr;
+                    const float o = (row + 1 <= 3) ? 0.f : 1.f;
+                    const float theta = o * s1 / fi;   // in units of the row maximum 2^0 = 1
+                    const float den = 1.f - theta;
+                    if (den > kDegenerateRel + kDegenerateAbs) {
+                        rc.kappa = 1.f / den;
+                        rc.beta = -theta * rc.kappa;
+                    } else {
+                        rc.kappa = 1.f;   // all-zero re-weighted row: (2^(z-m))^p ~= 1
+                        rc.beta = 0.f;
+                    }
+                } else if constexpr (MODE == kSigmoidRw) {
+                    const float s1 = bars->x_s1[w][0][t] + bars->x_s1[w][1][t];
+                    const float o = (row + 1 <= 3) ? 0.f : 1.f;
+                    const float theta = o * s1 / fi;
+                    const float sgm = ptx::rcp(1.f + ptx::ex2(-mxr));
+                    const float den = sgm - theta;
+                    if (den > kDegenerateRel * sgm + kDegenerateAbs) {
+                        rc.kappa = 1.f / den;
+                        rc.beta = -theta * rc.kappa;
+                    } else {
+                        rc.kappa = 1.f / sgm;   // all-zero re-weighted row
+                        rc.beta = 0.f;
+                    }
                 } else {
                     const float s1 = bars->x_s1[w][0][t] + bars->x_s1[w][1][t];
                     const float o = (row + 1 <= 3) ? 0.f : 1.f;
@@ -693,15 +801,15 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // is ready (d = 128: over S columns already loaded above)
                 {
                     uint32_t pk[16];
-                    if (kt == qt) to_z<true>(r0, 64 * h, t, rc.a);
-                    else to_z<false>(r0, 64 * h, t, rc.a);
+                    if (kt == qt) to_z<MODE, true>(r0, 64 * h, t, rc.a);
+                    else to_z<MODE, false>(r0, 64 * h, t, rc.a);
                     weights_z<MODE, PK>(r0, rc, prm.p, acc2[0], pk);
                     ptx::tmem_st16(p_col, pk);
                 }
                 {
                     uint32_t pk[16];
-                    if (kt == qt) to_z<true>(r1, 64 * h + 32, t, rc.a);
-                    else to_z<false>(r1, 64 * h + 32, t, rc.a);
+                    if (kt == qt) to_z<MODE, true>(r1, 64 * h + 32, t, rc.a);
+                    else to_z<MODE, false>(r1, 64 * h + 32, t, rc.a);
                     weights_z<MODE, PK>(r1, rc, prm.p, acc2[1], pk);
                     ptx::tmem_st16(p_col + 16, pk);
                 }

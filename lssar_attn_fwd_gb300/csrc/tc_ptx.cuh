@@ -258,6 +258,12 @@ __device__ __forceinline__ float lg2(float x) {
     return y;
 }
 
+__device__ __forceinline__ float rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Two floats to packed bf16x2 (round to nearest even): lo in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;

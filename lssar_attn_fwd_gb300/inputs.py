@@ -30,6 +30,8 @@ import numpy as np
 MODE_SOFTMAX = 0
 MODE_LSSA = 1
 MODE_LSSAR = 2
+MODE_SOFTMAX_RW = 3     # ablation: re-weighting on a softmax normaliser
+MODE_SIGMOID_RW = 4     # ablation: sigmoid + L1 + re-weighting
 
 
 @dataclass(frozen=True)

@@ -56,7 +56,7 @@ def call(lib, name="lssar_attn_fwd", q=Q, k=K, v=V, out=OUT, B=1, H=1, L=16, d=6
 def test_invalid_arguments(lib, name):
     assert call(lib, name, q=0) == -1
     assert call(lib, name, out=0) == -1
-    assert call(lib, name, mode=3) == -5
+    assert call(lib, name, mode=5) == -5
     assert call(lib, name, mode=-1) == -5
     assert call(lib, name, B=0) == -2
     assert call(lib, name, H=-1) == -2
@@ -67,6 +67,8 @@ def test_invalid_arguments(lib, name):
     assert call(lib, name, d=256) == -3
     assert call(lib, name, p=0) == -4
     assert call(lib, name, p=1025) == -4
+    assert call(lib, name, mode=3, p=0) == -4     # re-weighting on the softmax normaliser
+    assert call(lib, name, mode=4, p=0) == -4     # sigmoid + L1 + re-weighting
     assert call(lib, name, q=Q + 8) == -6
     assert call(lib, name, v=V + 2) == -6
     assert call(lib, name, out=Q + 1024) == -8   # out overlaps q

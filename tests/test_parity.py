@@ -12,14 +12,18 @@ import numpy as np
 import pytest
 
 from lssar_attn_fwd_gb300.inputs import (
-    MODE_LSSA, MODE_LSSAR, MODE_SOFTMAX, WORKLOADS, bf16_bits_to_f64, make_qkv, needle_targets)
+    MODE_LSSA, MODE_LSSAR, MODE_SIGMOID_RW, MODE_SOFTMAX, MODE_SOFTMAX_RW, WORKLOADS,
+    bf16_bits_to_f64, make_qkv, needle_targets)
 from oracle import attention_forward
 
 pytestmark = pytest.mark.gpu
 
 
+RW_MODES = (MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW)
+
+
 def tol(mode, p):
-    return 5e-2 if (mode == MODE_LSSAR and p >= 15) else 2e-2
+    return 5e-2 if (mode in RW_MODES and p >= 15) else 2e-2
 
 
 @pytest.fixture(scope="module")
@@ -50,7 +54,8 @@ def check_error_word():
 
 
 MODES = [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_LSSAR, 1), (MODE_LSSAR, 2), (MODE_LSSAR, 7),
-         (MODE_LSSA, 1), (MODE_SOFTMAX, 1)]
+         (MODE_LSSA, 1), (MODE_SOFTMAX, 1), (MODE_SOFTMAX_RW, 3), (MODE_SOFTMAX_RW, 15),
+         (MODE_SOFTMAX_RW, 1), (MODE_SIGMOID_RW, 3), (MODE_SIGMOID_RW, 15), (MODE_SIGMOID_RW, 2)]
 
 
 @pytest.mark.parametrize("mode,p", MODES)
@@ -69,7 +74,8 @@ def test_tiny_all_modes(torch_mod, mode, p):
 def test_ragged_lengths(torch_mod, L, d):
     qb, kb, vb = make_qkv(2, 2, L, d, seed=L + d)
     qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
-    for mode, p in [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_LSSA, 1), (MODE_SOFTMAX, 1)]:
+    for mode, p in [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_LSSA, 1), (MODE_SOFTMAX, 1),
+                    (MODE_SOFTMAX_RW, 15), (MODE_SIGMOID_RW, 3)]:
         got = run(torch_mod, qb, kb, vb, p, mode)
         ref = attention_forward(qf, kf, vf, mode, p)
         err = np.abs(got - ref).max()
@@ -84,7 +90,8 @@ def test_multi_pair_full_check(torch_mod, d):
     qb, kb, vb = make_qkv(B, H, L, d, seed=d)
     qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
     heads = [(0, 0), (1, 17), (2, 59)]
-    for mode, p in [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_SOFTMAX, 1), (MODE_LSSA, 1)]:
+    for mode, p in [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_SOFTMAX, 1), (MODE_LSSA, 1),
+                    (MODE_SOFTMAX_RW, 3), (MODE_SIGMOID_RW, 15)]:
         got = run(torch_mod, qb, kb, vb, p, mode)
         for b, h in heads:
             ref = attention_forward(qf[b, h], kf[b, h], vf[b, h], mode, p)
@@ -121,7 +128,8 @@ def test_rows_sum_to_one_full_size(torch_mod):
     w = WORKLOADS["extrap"]
     qb, kb, _ = make_qkv(*w.shape, seed=2)
     ones = np.full(w.shape, 0x3F80, dtype=np.uint16)   # bf16 1.0
-    for mode, p in [(MODE_LSSAR, 15), (MODE_LSSAR, 3), (MODE_LSSA, 1), (MODE_SOFTMAX, 1)]:
+    for mode, p in [(MODE_LSSAR, 15), (MODE_LSSAR, 3), (MODE_LSSA, 1), (MODE_SOFTMAX, 1),
+                    (MODE_SOFTMAX_RW, 15), (MODE_SIGMOID_RW, 15)]:
         got = run(torch_mod, qb, kb, ones, p, mode)
         assert np.abs(got - 1.0).max() <= 1e-2, mode
 
@@ -129,7 +137,8 @@ def test_rows_sum_to_one_full_size(torch_mod):
 def test_first_row_is_first_value(torch_mod):
     qb, kb, vb = make_qkv(2, 3, 384, 64, seed=5)
     vf = bf16_bits_to_f64(vb)
-    for mode, p in [(MODE_LSSAR, 15), (MODE_LSSA, 1), (MODE_SOFTMAX, 1)]:
+    for mode, p in [(MODE_LSSAR, 15), (MODE_LSSA, 1), (MODE_SOFTMAX, 1), (MODE_SOFTMAX_RW, 15),
+                    (MODE_SIGMOID_RW, 3)]:
         got = run(torch_mod, qb, kb, vb, p, mode)
         np.testing.assert_array_equal(got[:, :, 0], vf[:, :, 0])
 
@@ -142,7 +151,8 @@ def test_identical_keys_give_prefix_mean(torch_mod):
     kb = np.broadcast_to(kb[:, :, :1], kb.shape).copy()
     vf = bf16_bits_to_f64(vb)
     mean = np.cumsum(vf, axis=2) / np.arange(1, L + 1)[None, None, :, None]
-    for mode, p in [(MODE_LSSA, 1), (MODE_LSSAR, 3), (MODE_LSSAR, 15)]:
+    for mode, p in [(MODE_LSSA, 1), (MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_SOFTMAX_RW, 15),
+                    (MODE_SIGMOID_RW, 15)]:
         got = run(torch_mod, qb, kb, vb, p, mode)
         assert np.abs(got - mean).max() <= 2e-2, mode
 
@@ -174,10 +184,28 @@ def test_tc_matches_simt_full_size(torch_mod):
         assert np.abs(a - b).max() <= 2 * tol(mode, p)
 
 
+@pytest.mark.parametrize("name", ["extrap", "wide"])
+def test_ablation_modes_full_size_sampled_rows(torch_mod, name):
+    # The two ablation normalisers (notes' ablation table) at full size.
+    w = WORKLOADS[name]
+    qb, kb, vb = make_qkv(*w.shape, seed=10)
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    rows = sample_rows(w.L, seed=11)
+    for mode in (MODE_SOFTMAX_RW, MODE_SIGMOID_RW):
+        got = run(torch_mod, qb, kb, vb, 15, mode)
+        assert np.isfinite(got).all()
+        for b, h in [(0, 0), (w.B - 1, w.H - 1)]:
+            ref = attention_forward(qf[b, h], kf[b, h], vf[b, h], mode, 15, rows=rows)
+            err = np.abs(got[b, h, rows - 1] - ref).max()
+            assert err <= tol(mode, 15), (name, mode, b, h, err)
+    check_error_word()
+
+
 def test_simt_matches_oracle(torch_mod):
     qb, kb, vb = make_qkv(1, 2, 300, 128, seed=8)
     qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
-    for mode, p in [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_LSSA, 1), (MODE_SOFTMAX, 1)]:
+    for mode, p in [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_LSSA, 1), (MODE_SOFTMAX, 1),
+                    (MODE_SOFTMAX_RW, 15), (MODE_SIGMOID_RW, 15)]:
         got = run(torch_mod, qb, kb, vb, p, mode, "simt")
         ref = attention_forward(qf, kf, vf, mode, p)
         assert np.abs(got - ref).max() <= tol(mode, p)
