@@ -80,6 +80,21 @@ int lssar_attn_fwd(const void *q, const void *k, const void *v, void *out,
                    int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
 
 /*
+ * lssar_attn_fwd with one re-weighting exponent per head: head h (of every
+ * batch entry) uses p_per_head[h].  The notes leave an adaptive or learnable p
+ * open (Limitations: p = 15 is empirical; Key findings: the best sparsity
+ * depends on the length); a per-head p is what such a model needs at
+ * inference time.
+ *   p_per_head : HOST array of H ints, each in 1..1024, read before return.
+ *   mode       : a re-weighting mode (2, 3 or 4); other modes return
+ *                LSSAR_ERR_P.  H must be at most 256 (LSSAR_ERR_P otherwise).
+ * Other arguments, results and errors as lssar_attn_fwd.
+ */
+int lssar_attn_fwd_heads_p(const void *q, const void *k, const void *v, void *out,
+                           int B, int H, int L, int d, const int *p_per_head, int mode,
+                           cudaStream_t stream);
+
+/*
  * Same operation and contract as lssar_attn_fwd, computed by a plain CUDA-core
  * kernel (one warp per query row, fp32 throughout, accurate libm softplus).
  * It is a second, independent GPU implementation kept for cross-checking the

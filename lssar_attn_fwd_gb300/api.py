@@ -19,6 +19,7 @@ _EXPORTS = (
     "lssar_attn_fwd_simt",
     "lssar_attn_fwd_profiled",
     "lssar_attn_fwd_noalloc",
+    "lssar_attn_fwd_heads_p",
     "lssar_status_string",
     "lssar_device_error_word",
     "lssar_abi_version",
@@ -51,6 +52,9 @@ def load_library():
         fn = getattr(lib, name)
         fn.argtypes = fwd_args
         fn.restype = ctypes.c_int
+    lib.lssar_attn_fwd_heads_p.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 +
+                                           [ctypes.POINTER(ctypes.c_int), ctypes.c_int, ctypes.c_void_p])
+    lib.lssar_attn_fwd_heads_p.restype = ctypes.c_int
     lib.lssar_attn_fwd_profiled.argtypes = fwd_args + [ctypes.c_void_p] * 3
     lib.lssar_attn_fwd_profiled.restype = ctypes.c_int
     lib.lssar_status_string.argtypes = [ctypes.c_int]
@@ -121,6 +125,31 @@ def lssar_attn_fwd(q, k, v, p=3, mode=MODE_LSSAR, out=None, stream=None):
 def lssar_attn_fwd_simt(q, k, v, p=3, mode=MODE_LSSAR, out=None, stream=None):
     """Same operation on the plain CUDA-core kernel (cross-check only)."""
     return _forward("lssar_attn_fwd_simt", q, k, v, p, mode, out, stream)
+
+
+def call_heads_p(q_ptr, k_ptr, v_ptr, out_ptr, B, H, L, d, p_per_head, mode, stream_handle):
+    """Raw call of lssar_attn_fwd_heads_p; returns the status."""
+    arr = (ctypes.c_int * max(1, len(p_per_head)))(*[int(x) for x in p_per_head])
+    ptr = arr if len(p_per_head) else None
+    return load_library().lssar_attn_fwd_heads_p(
+        ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+        ctypes.c_void_p(out_ptr), int(B), int(H), int(L), int(d), ptr, int(mode),
+        ctypes.c_void_p(stream_handle))
+
+
+def lssar_attn_fwd_heads_p(q, k, v, p_per_head, mode=MODE_LSSAR, out=None, stream=None):
+    """Re-weighting modes with one exponent per head (p_per_head: H ints)."""
+    import torch
+    B, H, L, d = q.shape
+    if len(p_per_head) != H:
+        raise ValueError("p_per_head must hold one exponent per head")
+    if out is None:
+        out = torch.empty_like(q)
+    with torch.cuda.device(q.device):
+        s = torch.cuda.current_stream(q.device) if stream is None else stream
+        _check(call_heads_p(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            B, H, L, d, p_per_head, mode, s.cuda_stream))
+    return out
 
 
 def lssar_attn_fwd_profiled(q, k, v, p, mode, out, stream, ev_start, ev_main, ev_end):

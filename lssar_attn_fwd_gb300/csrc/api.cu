@@ -11,6 +11,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxP = 1024;
+constexpr int kMaxHeadsP = 256;   // = tc::kMaxHeadsP
 
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
     const auto x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -109,6 +110,31 @@ int lssar_attn_fwd_profiled(const void *q, const void *k, const void *v, void *o
     ev.main = ev_main;
     ev.end = ev_end;
     return run_tc(q, k, v, out, B, H, L, d, p, mode, stream, ev);
+}
+
+int lssar_attn_fwd_heads_p(const void *q, const void *k, const void *v, void *out, int B, int H,
+                           int L, int d, const int *p_per_head, int mode, cudaStream_t stream) {
+    if (!p_per_head) return LSSAR_ERR_NULL;
+    if (!lssar::is_reweight(mode)) {
+        if (mode < LSSAR_MODE_SOFTMAX || mode > LSSAR_MODE_SIGMOID_RW) return LSSAR_ERR_MODE;
+        return LSSAR_ERR_P;   // per-head exponents need a re-weighting mode
+    }
+    if (H < 1) return LSSAR_ERR_SHAPE;
+    if (H > kMaxHeadsP) return LSSAR_ERR_P;
+    for (int h = 0; h < H; ++h)
+        if (p_per_head[h] < 1 || p_per_head[h] > kMaxP) return LSSAR_ERR_P;
+    lssar::Problem pr;
+    const int st = validate(q, k, v, out, B, H, L, d, p_per_head[0], mode, &pr);
+    if (st != LSSAR_OK) return st;
+    pr.p_head = p_per_head;
+    const size_t ws_bytes = lssar::tc_workspace_bytes(pr);
+    void *ws = nullptr;
+    cudaMemPool_t pool;
+    if (device_pool(&pool) != cudaSuccess) return LSSAR_ERR_CUDA;
+    if (cudaMallocFromPoolAsync(&ws, ws_bytes, pool, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    const cudaError_t e = lssar::launch_tc(pr, ws, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
 }
 
 int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out, int B, int H,

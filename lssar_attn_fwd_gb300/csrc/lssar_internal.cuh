@@ -20,10 +20,11 @@ struct Problem {
     const void *v;
     void *out;
     int B, H, L, d, p, mode;
+    const int *p_head = nullptr;   // host array of H exponents, or null (one p for all heads)
 };
 
 // Host-side argument checks of the C ABI (no CUDA call); LSSAR_OK or a
-// negative status.  Fills *pr on success.
+// negative status.  Fills *pr on success (p_head left null).
 int validate_args(const void *q, const void *k, const void *v, void *out, int B, int H, int L,
                   int d, int p, int mode, Problem *pr);
 

@@ -37,6 +37,7 @@ cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CU
 template <int D, int MODE>
 cudaError_t dispatch_p(const Problem &pr, const CUtensorMap &mq, const CUtensorMap &mk,
                        const CUtensorMap &mv, const Params &prm, int grid, cudaStream_t s) {
+    if (pr.p_head) return launch_kernel<D, MODE, 0>(mq, mk, mv, prm, grid, s);   // per head
     switch (pr.p) {
         case 1: return launch_kernel<D, MODE, 1>(mq, mk, mv, prm, grid, s);
         case 2: return launch_kernel<D, MODE, 2>(mq, mk, mv, prm, grid, s);

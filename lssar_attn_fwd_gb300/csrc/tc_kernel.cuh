@@ -95,6 +95,8 @@ constexpr uint32_t kKmajorSbo = 1024;
 constexpr uint32_t kVLbo = 16384;
 constexpr uint32_t kVSbo = 1024;
 
+constexpr int kMaxHeadsP = 256;   // per-head exponents carried in the kernel parameters
+
 struct Params {
     int BH;          // B * H
     int L;
@@ -102,7 +104,10 @@ struct Params {
     int n_pairs;     // ceil(n_qtiles / 2)
     int n_items;     // BH * n_pairs
     float ln_d;      // ln(d)
-    int p;           // LSSAR exponent (used by the generic power path)
+    int p;           // re-weighting exponent (used by the generic power path)
+    int H;           // heads per batch entry (for the per-head exponents)
+    int per_head;    // 1: head h uses p_head[h] (generic power path only)
+    int p_head[kMaxHeadsP];
     __nv_bfloat16 *out;
     unsigned *err;       // device error word
     unsigned *counter;   // work counter, zero at launch
@@ -666,6 +671,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int n = qt + 1;
             const int row = qt * kBM + t;
             const float fi = (float)(row + 1);
+            const int p_row = (PK == 0 && prm.per_head) ? prm.p_head[bh % prm.H] : prm.p;
             RowConst rc;
             if constexpr (kRawQK)
                 rc.a = log2e * rsqrtf((float)D);
@@ -803,14 +809,14 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     uint32_t pk[16];
                     if (kt == qt) to_z<MODE, true>(r0, 64 * h, t, rc.a);
                     else to_z<MODE, false>(r0, 64 * h, t, rc.a);
-                    weights_z<MODE, PK>(r0, rc, prm.p, acc2[0], pk);
+                    weights_z<MODE, PK>(r0, rc, p_row, acc2[0], pk);
                     ptx::tmem_st16(p_col, pk);
                 }
                 {
                     uint32_t pk[16];
                     if (kt == qt) to_z<MODE, true>(r1, 64 * h + 32, t, rc.a);
                     else to_z<MODE, false>(r1, 64 * h + 32, t, rc.a);
-                    weights_z<MODE, PK>(r1, rc, prm.p, acc2[1], pk);
+                    weights_z<MODE, PK>(r1, rc, p_row, acc2[1], pk);
                     ptx::tmem_st16(p_col + 16, pk);
                 }
                 ptx::tmem_st_wait();

@@ -96,3 +96,17 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(api, "lib_path", lambda: "/nonexistent/liblssar_attn_fwd.so")
     with pytest.raises(RuntimeError, match="no fallback"):
         api.load_library()
+
+
+def test_heads_p_invalid_arguments(lib):
+    from lssar_attn_fwd_gb300.api import call_heads_p
+    good = [3, 15]
+    assert call_heads_p(Q, K, V, OUT, 1, 2, 16, 64, [], 2, 0) == -1          # no array
+    assert call_heads_p(Q, K, V, OUT, 1, 2, 16, 64, good, 0, 0) == -4        # softmax: no p
+    assert call_heads_p(Q, K, V, OUT, 1, 2, 16, 64, good, 1, 0) == -4        # LSSA: no p
+    assert call_heads_p(Q, K, V, OUT, 1, 2, 16, 64, good, 9, 0) == -5
+    assert call_heads_p(Q, K, V, OUT, 1, 2, 16, 64, [3, 0], 2, 0) == -4
+    assert call_heads_p(Q, K, V, OUT, 1, 2, 16, 64, [3, 2000], 3, 0) == -4
+    assert call_heads_p(Q, K, V, OUT, 1, 300, 16, 64, [3] * 300, 2, 0) == -4  # > 256 heads
+    assert call_heads_p(Q, K, V, OUT, 1, 2, 16, 96, good, 4, 0) == -3
+    assert call_heads_p(Q + 4, K, V, OUT, 1, 2, 16, 64, good, 2, 0) == -6

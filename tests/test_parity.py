@@ -201,6 +201,29 @@ def test_ablation_modes_full_size_sampled_rows(torch_mod, name):
     check_error_word()
 
 
+@pytest.mark.parametrize("mode", [MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW])
+@pytest.mark.parametrize("d", [64, 128])
+def test_per_head_exponents(torch_mod, mode, d):
+    # lssar_attn_fwd_heads_p: head h uses its own p; each head must match the
+    # oracle at that p.
+    torch = torch_mod
+    from lssar_attn_fwd_gb300 import api
+    B, H, L = 2, 5, 300
+    ps = [1, 3, 15, 40, 2]
+    qb, kb, vb = make_qkv(B, H, L, d, seed=12)
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    q, k, v = (to_dev(torch, t) for t in (qb, kb, vb))
+    got = api.lssar_attn_fwd_heads_p(q, k, v, ps, mode=mode)
+    torch.cuda.synchronize()
+    got = got.float().cpu().numpy().astype(np.float64)
+    for b in range(B):
+        for h in range(H):
+            ref = attention_forward(qf[b, h], kf[b, h], vf[b, h], mode, ps[h])
+            err = np.abs(got[b, h] - ref).max()
+            assert err <= tol(mode, ps[h]), (mode, d, b, h, ps[h], err)
+    check_error_word()
+
+
 def test_simt_matches_oracle(torch_mod):
     qb, kb, vb = make_qkv(1, 2, 300, 128, seed=8)
     qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
