@@ -353,6 +353,50 @@ def run_ours(args, wl, mode, p):
         dist.destroy_process_group()
 
 
+def run_decode(args, mode, p):
+    """Decode step: one query per head (position L) against a K/V cache,
+    B=8 H=12 L=16384 d=64 unless overridden.  Bound by HBM: the metric is the
+    K/V cache bytes read per second against the measured copy bandwidth."""
+    import torch
+    from lssar_attn_fwd_gb300 import api
+    from lssar_attn_fwd_gb300.build import build
+    build()
+    api.load_library()
+    B, H, L, d = args.decode_shape
+    qb, kb, vb = make_qkv(B, H, L, d, seed=0)
+    to_t = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    q, k, v = to_t(qb[:, :, -1]), to_t(kb), to_t(vb)
+    out = torch.empty_like(q)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        api.lssar_attn_decode(q, k, v, p=p, mode=mode, out=out)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record(s)
+        api.lssar_attn_decode(q, k, v, p=p, mode=mode, out=out)
+        b.record(s)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    cache_bytes = 2 * B * H * L * d * 2
+    gbs = cache_bytes / (ms * 1e-3) / 1e9
+    try:
+        peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
+        kind = "measured"
+    except Exception:
+        peak, kind = 6800.0, "fallback"
+    print(json.dumps({
+        "metric": "LSSAR decode step: K/V cache bytes read per second", "value": gbs, "unit": "GB/s",
+        "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "config": {"workload": f"decode: B={B} H={H} L={L} d={d} mode={mode} p={p}, one query per head",
+                   "l2": "flushed before every step (256 MiB write)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_source": f"{kind} hbm_gbs"},
+        "gpu_launches": 3 * args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -364,6 +408,9 @@ def main():
     ap.add_argument("--p", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true", help="benchmark the decode step instead")
+    ap.add_argument("--decode-shape", type=int, nargs=4, default=[8, 12, 16384, 64],
+                    metavar=("B", "H", "L", "D"))
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -373,7 +420,9 @@ def main():
         mode = MODE_NAMES[args.mode]
     if args.p is not None:
         p = args.p
-    if args.impl == "reference":
+    if args.decode:
+        run_decode(args, mode, p)
+    elif args.impl == "reference":
         run_reference(args, wl, mode, p)
     else:
         run_ours(args, wl, mode, p)

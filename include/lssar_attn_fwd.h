@@ -95,6 +95,22 @@ int lssar_attn_fwd_heads_p(const void *q, const void *k, const void *v, void *ou
                            cudaStream_t stream);
 
 /*
+ * Decode step: the forward for ONE new query row per head, at position L
+ * (1-based, i.e. it attends to all L cached tokens, itself included), for
+ * every mode above.  Equal to row L of lssar_attn_fwd on the full sequence
+ * (the notes evaluate a model trained at 1K tokens at 2K-8K: this is that
+ * inference step).
+ *   q       : [B, H, d] bfloat16, device (the new token's query).
+ *   k_cache : [B, H, L, d] bfloat16, device (keys 1..L, the new one last).
+ *   v_cache : [B, H, L, d] bfloat16, device.
+ *   out     : [B, H, d] bfloat16, device, written.
+ * Bound by HBM: K and V are read once (scores are kept in a float scratch of
+ * 4*B*H*L bytes between the passes).  Same errors as lssar_attn_fwd.
+ */
+int lssar_attn_decode(const void *q, const void *k_cache, const void *v_cache, void *out,
+                      int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
+
+/*
  * Same operation and contract as lssar_attn_fwd, computed by a plain CUDA-core
  * kernel (one warp per query row, fp32 throughout, accurate libm softplus).
  * It is a second, independent GPU implementation kept for cross-checking the

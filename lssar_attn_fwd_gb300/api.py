@@ -20,6 +20,7 @@ _EXPORTS = (
     "lssar_attn_fwd_profiled",
     "lssar_attn_fwd_noalloc",
     "lssar_attn_fwd_heads_p",
+    "lssar_attn_decode",
     "lssar_status_string",
     "lssar_device_error_word",
     "lssar_abi_version",
@@ -48,7 +49,7 @@ def load_library():
             "(there is no fallback implementation)")
     lib = ctypes.CDLL(path)
     fwd_args = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
-    for name in ("lssar_attn_fwd", "lssar_attn_fwd_simt", "lssar_attn_fwd_noalloc"):
+    for name in ("lssar_attn_fwd", "lssar_attn_fwd_simt", "lssar_attn_fwd_noalloc", "lssar_attn_decode"):
         fn = getattr(lib, name)
         fn.argtypes = fwd_args
         fn.restype = ctypes.c_int
@@ -149,6 +150,28 @@ def lssar_attn_fwd_heads_p(q, k, v, p_per_head, mode=MODE_LSSAR, out=None, strea
         s = torch.cuda.current_stream(q.device) if stream is None else stream
         _check(call_heads_p(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                             B, H, L, d, p_per_head, mode, s.cuda_stream))
+    return out
+
+
+def lssar_attn_decode(q, k_cache, v_cache, p=3, mode=MODE_LSSAR, out=None, stream=None):
+    """One new query row per head (position L) against a K/V cache.
+
+    q: [B, H, d] bf16; k_cache, v_cache: [B, H, L, d] bf16 (contiguous, CUDA).
+    Returns out [B, H, d] bf16, equal to row L of the full causal forward.
+    """
+    import torch
+    for t in (q, k_cache, v_cache):
+        if t.device.type != "cuda" or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k_cache, v_cache must be contiguous bfloat16 CUDA tensors")
+    B, H, L, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or tuple(q.shape) != (B, H, d):
+        raise ValueError("shapes must be q [B, H, d] and caches [B, H, L, d]")
+    if out is None:
+        out = torch.empty_like(q)
+    with torch.cuda.device(q.device):
+        s = torch.cuda.current_stream(q.device) if stream is None else stream
+        _check(call_raw("lssar_attn_decode", q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                        out.data_ptr(), B, H, L, d, p, mode, s.cuda_stream))
     return out
 
 

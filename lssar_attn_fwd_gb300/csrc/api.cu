@@ -137,6 +137,38 @@ int lssar_attn_fwd_heads_p(const void *q, const void *k, const void *v, void *ou
     return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
 }
 
+int lssar_attn_decode(const void *q, const void *k_cache, const void *v_cache, void *out, int B,
+                      int H, int L, int d, int p, int mode, cudaStream_t stream) {
+    if (!q || !k_cache || !v_cache || !out) return LSSAR_ERR_NULL;
+    if (mode < LSSAR_MODE_SOFTMAX || mode > LSSAR_MODE_SIGMOID_RW) return LSSAR_ERR_MODE;
+    if (B < 1 || H < 1 || L < 1 || L > (1 << 24)) return LSSAR_ERR_SHAPE;
+    if (d != 64 && d != 128) return LSSAR_ERR_HEADDIM;
+    const unsigned long long cache_elems = (unsigned long long)B * H * L * d;
+    if (cache_elems > (1ULL << 40)) return LSSAR_ERR_SHAPE;
+    const bool reweight = lssar::is_reweight(mode);
+    if (reweight && (p < 1 || p > kMaxP)) return LSSAR_ERR_P;
+    for (const void *ptr : {q, k_cache, v_cache, static_cast<const void *>(out)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15u) return LSSAR_ERR_ALIGN;
+    const size_t row_bytes = (size_t)B * H * d * 2, cache_bytes = (size_t)cache_elems * 2;
+    if (ranges_overlap(out, row_bytes, q, row_bytes) || ranges_overlap(out, row_bytes, k_cache, cache_bytes) ||
+        ranges_overlap(out, row_bytes, v_cache, cache_bytes))
+        return LSSAR_ERR_ALIAS;
+    lssar::DecodeProblem pr{q, k_cache, v_cache, out, B, H, L, d, reweight ? p : 1, mode};
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return LSSAR_ERR_CUDA;
+    cudaMemPool_t pool;
+    if (device_pool(&pool) != cudaSuccess) return LSSAR_ERR_CUDA;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, lssar::decode_workspace_bytes(B * H, L, d, sms), pool, stream) !=
+        cudaSuccess)
+        return LSSAR_ERR_CUDA;
+    const cudaError_t e = lssar::launch_decode(pr, ws, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
+}
+
 int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out, int B, int H,
                         int L, int d, int p, int mode, cudaStream_t stream) {
     lssar::Problem pr;

@@ -43,6 +43,17 @@ struct Events {
 size_t tc_workspace_bytes(const Problem &pr);
 cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Events &ev = Events());
 
+// Decode: one query row per head (position L) against a K/V cache of L rows.
+struct DecodeProblem {
+    const void *q;   // [B, H, d]
+    const void *k;   // [B, H, L, d]
+    const void *v;   // [B, H, L, d]
+    void *out;       // [B, H, d]
+    int B, H, L, d, p, mode;
+};
+size_t decode_workspace_bytes(int BH, int L, int d, int sms);
+cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream);
+
 // Reads and clears the device error word of the current device.
 cudaError_t read_and_clear_error_word(unsigned int *word);
 

@@ -110,3 +110,15 @@ def test_heads_p_invalid_arguments(lib):
     assert call_heads_p(Q, K, V, OUT, 1, 300, 16, 64, [3] * 300, 2, 0) == -4  # > 256 heads
     assert call_heads_p(Q, K, V, OUT, 1, 2, 16, 96, good, 4, 0) == -3
     assert call_heads_p(Q + 4, K, V, OUT, 1, 2, 16, 64, good, 2, 0) == -6
+
+
+def test_decode_invalid_arguments(lib):
+    from lssar_attn_fwd_gb300.api import call_raw
+    f = "lssar_attn_decode"
+    assert call_raw(f, 0, K, V, OUT, 1, 2, 16, 64, 3, 2, 0) == -1
+    assert call_raw(f, Q, K, V, OUT, 1, 2, 16, 64, 3, 7, 0) == -5
+    assert call_raw(f, Q, K, V, OUT, 1, 2, 0, 64, 3, 2, 0) == -2
+    assert call_raw(f, Q, K, V, OUT, 1, 2, 16, 32, 3, 2, 0) == -3
+    assert call_raw(f, Q, K, V, OUT, 1, 2, 16, 64, 0, 3, 0) == -4
+    assert call_raw(f, Q, K + 2, V, OUT, 1, 2, 16, 64, 3, 2, 0) == -6
+    assert call_raw(f, Q, K, V, K + 64, 1, 2, 16, 64, 3, 2, 0) == -8   # out inside the key cache

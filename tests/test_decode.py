@@ -1,0 +1,75 @@
+"""GPU parity of the decode forward (one query row per head at position L)
+against row L of the float64 oracle."""
+
+import numpy as np
+import pytest
+
+from lssar_attn_fwd_gb300.inputs import (
+    MODE_LSSA, MODE_LSSAR, MODE_SIGMOID_RW, MODE_SOFTMAX, MODE_SOFTMAX_RW,
+    bf16_bits_to_f64, make_qkv)
+from oracle import attention_forward
+
+pytestmark = pytest.mark.gpu
+
+ALL = [(MODE_SOFTMAX, 1), (MODE_LSSA, 1), (MODE_LSSAR, 3), (MODE_LSSAR, 15),
+       (MODE_SOFTMAX_RW, 15), (MODE_SIGMOID_RW, 15), (MODE_LSSAR, 64)]
+
+
+def tol(mode, p):
+    return 5e-2 if (mode in (MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW) and p >= 15) else 2e-2
+
+
+@pytest.fixture(scope="module")
+def torch_mod():
+    import torch
+    from lssar_attn_fwd_gb300 import api, build
+    build.build()
+    api.load_library()
+    return torch
+
+
+def decode(torch, qb, kb, vb, p, mode):
+    from lssar_attn_fwd_gb300 import api
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    q_last = dev(qb[:, :, -1])
+    out = api.lssar_attn_decode(q_last, dev(kb), dev(vb), p=p, mode=mode)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 255, 1000, 4097, 9000])
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_matches_last_row(torch_mod, L, d):
+    B, H = 2, 3
+    qb, kb, vb = make_qkv(B, H, L, d, seed=L + d)
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    for mode, p in ALL:
+        got = decode(torch_mod, qb, kb, vb, p, mode)
+        for b in range(B):
+            for h in range(H):
+                ref = attention_forward(qf[b, h], kf[b, h], vf[b, h], mode, p, rows=np.array([L]))[0]
+                err = np.abs(got[b, h] - ref).max()
+                assert err <= tol(mode, p), (L, d, mode, p, b, h, err)
+
+
+def test_decode_needle_16k(torch_mod):
+    B, H, L, d = 1, 12, 16384, 64
+    qb, kb, vb = make_qkv(B, H, L, d, seed=0, structure="needle")
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    got = decode(torch_mod, qb, kb, vb, 15, MODE_LSSAR)
+    for h in range(H):
+        ref = attention_forward(qf[0, h], kf[0, h], vf[0, h], MODE_LSSAR, 15, rows=np.array([L]))[0]
+        assert np.abs(got[0, h] - ref).max() <= 5e-2
+
+
+def test_decode_equals_prefill_last_row(torch_mod):
+    # the decode entry and the prefill kernel agree on row L
+    torch = torch_mod
+    from lssar_attn_fwd_gb300 import api
+    qb, kb, vb = make_qkv(2, 4, 1500, 64, seed=9)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    full = api.lssar_attn_fwd(dev(qb), dev(kb), dev(vb), p=15, mode=MODE_LSSAR)
+    torch.cuda.synchronize()
+    last = full[:, :, -1].float().cpu().numpy()
+    got = decode(torch, qb, kb, vb, 15, MODE_LSSAR)
+    assert np.abs(got - last).max() <= 5e-2
