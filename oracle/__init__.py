@@ -27,3 +27,4 @@ from .lssar_oracle import (  # noqa: F401
     attention_forward,
 )
 from .bruteforce import attention_bruteforce  # noqa: F401
+from .lssar_backward import attention_backward, head_backward  # noqa: F401
