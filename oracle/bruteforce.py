@@ -50,7 +50,8 @@ def attention_bruteforce(q, k, v, mode, p=3, o_override=None):
             a = [x / z for x in a]
         if mode in (MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW):
             o = (0.0 if i <= 3 else 1.0) if o_override is None else float(o_override)
-            r = [max(i * x - o, 0.0) ** p for x in a]
+            # ReLU; residues of 0 left by rounding (at most 1e-10) are 0
+            r = [(i * x - o) ** p if i * x - o > 1e-10 else 0.0 for x in a]
             t = sum(r)
             w = [x / t for x in r] if t > 0.0 else [1.0 / i] * i
         else:

@@ -41,7 +41,7 @@ import math
 import numpy as np
 
 from .lssar_oracle import (MODE_LSSA, MODE_LSSAR, MODE_SIGMOID_RW, MODE_SOFTMAX,
-                           MODE_SOFTMAX_RW, NORM_EPS, bias_o, length_scale, sigmoid,
+                           MODE_SOFTMAX_RW, NORM_EPS, Y_ZERO, bias_o, length_scale, sigmoid,
                            softplus)
 
 _REWEIGHT = (MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW)
@@ -74,7 +74,9 @@ def _reweight_backward(A, dR, rows, p, o_rows):
         np.asarray(o_rows, dtype=np.float64), rows.shape)
     i = rows[:, None].astype(np.float64)
     causal = np.arange(1, A.shape[1] + 1)[None, :] <= rows[:, None]
-    y = np.maximum(i * A - o[:, None], 0.0)
+    y = i * A - o[:, None]
+    active = y > Y_ZERO                               # the forward's ReLU (residues of 0 are 0)
+    y = np.where(active, y, 0.0)
     ymax = y.max(axis=1)
     R = causal / i
     dA = np.zeros_like(A)
@@ -86,9 +88,8 @@ def _reweight_backward(A, dR, rows, p, o_rows):
         Rk = r / rs
         R[ok] = Rk
         dr = (dR[ok] - np.sum(Rk * dR[ok], axis=1, keepdims=True)) / rs
-        active = (i[ok] * A[ok] - o[ok, None]) > 0.0
         slope = int(p) * t ** (int(p) - 1) / ymax[ok, None]
-        dA[ok] = i[ok] * active * slope * dr
+        dA[ok] = i[ok] * active[ok] * slope * dr
     return R, dA
 
 

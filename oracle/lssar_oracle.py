@@ -48,6 +48,12 @@ MODE_SIGMOID_RW = 4     # ablation: sigmoid + L1 + re-weighting
 
 NORM_EPS = 1e-12
 
+# A re-weighting input y = i*A - O at or below this counts as zero.  In exact
+# arithmetic a uniform LSSA row (the 0/0 case) has y = 0 on every entry; its
+# float64 evaluation leaves residues of the order of i * 2^-53 of either sign,
+# which the power p would otherwise turn into an arbitrary selection.
+Y_ZERO = 1e-10
+
 
 def softplus(x):
     """Softplus(x) = log(1 + e^x)  [Key design 1: Softplus replaces e^x].
@@ -126,7 +132,8 @@ def reweight_rows(a, rows, p, o_rows=None):
     p:      integer exponent >= 1.
     o_rows: optional per-row override of O (used only by tests, e.g. O = 0).
 
-    ``y = max(i*a - O, 0)`` and the result is ``(y/max_j y)^p`` normalised:
+    ``y = max(i*a - O, 0)`` (values at or below ``Y_ZERO`` are rounding
+    residues of 0) and the result is ``(y/max_j y)^p`` normalised:
     dividing by the row maximum first is a common factor that the L1
     normalisation cancels, and it keeps large p inside float64 range.  A row
     with ``max_j y == 0`` is degenerate (0/0) and is read as the uniform
@@ -137,7 +144,8 @@ def reweight_rows(a, rows, p, o_rows=None):
         o = bias_o(rows)
     else:
         o = np.broadcast_to(np.asarray(o_rows, dtype=np.float64), rows.shape)
-    y = np.maximum(rows[:, None] * a - o[:, None], 0.0)
+    y = rows[:, None] * a - o[:, None]
+    y = np.where(y > Y_ZERO, y, 0.0)              # ReLU, with rounding residues of 0 taken as 0
     ymax = y.max(axis=1)
     out = _causal(rows, a.shape[1]) / rows[:, None].astype(np.float64)
     ok = ymax > 0.0
