@@ -61,7 +61,7 @@ typedef enum {
     LSSAR_ERR_MODE = -5,    /* unknown mode                                           */
     LSSAR_ERR_ALIGN = -6,   /* a pointer is not 16-byte aligned                       */
     LSSAR_ERR_CUDA = -7,    /* a CUDA call failed (launch, pool allocation, ...)      */
-    LSSAR_ERR_ALIAS = -8,   /* out overlaps q, k or v                                 */
+    LSSAR_ERR_ALIAS = -8,   /* an output overlaps an input (or another output)         */
     LSSAR_ERR_SCRATCH = -9  /* lssar_attn_fwd_noalloc: problem needs more scratch than
                                LSSAR_NOALLOC_SCRATCH_BYTES                            */
 } lssar_status_t;
@@ -93,6 +93,46 @@ int lssar_attn_fwd(const void *q, const void *k, const void *v, void *out,
 int lssar_attn_fwd_heads_p(const void *q, const void *k, const void *v, void *out,
                            int B, int H, int L, int d, const int *p_per_head, int mode,
                            cudaStream_t stream);
+
+/*
+ * Training forward: lssar_attn_fwd that also saves, per query row, what the
+ * backward pass needs (the notes train GPT-2 models with this attention).
+ *   stats : [B, H, L, 4] float32, device, 16-byte aligned, written:
+ *           {m, kappa, beta, W} per row, in the kernel's log2 units
+ *           (z = log2(e) * x):  phi(z) = log2(1 + 2^z) (LSSA/LSSAR),
+ *           2^(z - m) (softmax normalisers), 1/(1 + 2^-z) (sigmoid); the row's
+ *           weights are w = max(phi kappa + beta, 0)^p with W = sum_j w
+ *           (kappa = 1, beta = 0, p = 1 without re-weighting).  A row read as
+ *           the uniform prefix mean has kappa = 0, beta = 1, W = i.
+ * Must not overlap q, k, v or out.  Other arguments, results and errors as
+ * lssar_attn_fwd (LSSAR_ERR_NULL for a NULL stats, LSSAR_ERR_ALIGN, ALIAS).
+ */
+int lssar_attn_fwd_train(const void *q, const void *k, const void *v, void *out, float *stats,
+                         int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
+
+/*
+ * Backward pass: gradients of sum(dout * out) with respect to q, k and v,
+ * given the row statistics of the forward (lssar_attn_fwd_train with the same
+ * q, k, v, B, H, L, d, p, mode).  Chain rule through the steps of Key designs
+ * 1-2: the derivative of the L1 normalisations, of the re-weighting threshold
+ * (its row sum S1), of softplus / sigmoid / exp and of the L2 row
+ * normalisation; a uniform row passes no gradient to its scores.  The
+ * forward's output is not needed: dout_i . out_i is formed from the
+ * recomputed weights, free of the output's bf16 rounding.
+ *   q, k, v, dout : [B, H, L, d] bfloat16, device, read only.
+ *   stats         : [B, H, L, 4] float32 from lssar_attn_fwd_train.
+ *   dq, dk, dv    : [B, H, L, d] bfloat16, device, written; they must not
+ *                   overlap each other or any input (LSSAR_ERR_ALIAS).
+ * Scratch (8*B*H*L bytes) comes from the library's stream-ordered pool.  Other
+ * arguments and errors as lssar_attn_fwd.
+ *
+ * This entry point runs a plain CUDA-core implementation (one warp per query
+ * row for dq, one warp per key row for dk and dv, fp32, libm
+ * transcendentals); it is the cross-check for the tensor-core backward.
+ */
+int lssar_attn_bwd_simt(const void *q, const void *k, const void *v, const void *dout,
+                        const float *stats, void *dq, void *dk, void *dv,
+                        int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
 
 /*
  * Decode step: the forward for ONE new query row per head, at position L

@@ -21,6 +21,8 @@ _EXPORTS = (
     "lssar_attn_fwd_noalloc",
     "lssar_attn_fwd_heads_p",
     "lssar_attn_decode",
+    "lssar_attn_fwd_train",
+    "lssar_attn_bwd_simt",
     "lssar_status_string",
     "lssar_device_error_word",
     "lssar_abi_version",
@@ -56,6 +58,12 @@ def load_library():
     lib.lssar_attn_fwd_heads_p.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 +
                                            [ctypes.POINTER(ctypes.c_int), ctypes.c_int, ctypes.c_void_p])
     lib.lssar_attn_fwd_heads_p.restype = ctypes.c_int
+    lib.lssar_attn_fwd_train.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
+    lib.lssar_attn_fwd_train.restype = ctypes.c_int
+    for name in ("lssar_attn_bwd_simt",):
+        fn = getattr(lib, name)
+        fn.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
+        fn.restype = ctypes.c_int
     lib.lssar_attn_fwd_profiled.argtypes = fwd_args + [ctypes.c_void_p] * 3
     lib.lssar_attn_fwd_profiled.restype = ctypes.c_int
     lib.lssar_status_string.argtypes = [ctypes.c_int]
@@ -126,6 +134,73 @@ def lssar_attn_fwd(q, k, v, p=3, mode=MODE_LSSAR, out=None, stream=None):
 def lssar_attn_fwd_simt(q, k, v, p=3, mode=MODE_LSSAR, out=None, stream=None):
     """Same operation on the plain CUDA-core kernel (cross-check only)."""
     return _forward("lssar_attn_fwd_simt", q, k, v, p, mode, out, stream)
+
+
+def call_train(q_ptr, k_ptr, v_ptr, out_ptr, stats_ptr, B, H, L, d, p, mode, stream_handle):
+    """Raw call of lssar_attn_fwd_train; returns the status."""
+    return load_library().lssar_attn_fwd_train(
+        *(ctypes.c_void_p(x) for x in (q_ptr, k_ptr, v_ptr, out_ptr, stats_ptr)),
+        int(B), int(H), int(L), int(d), int(p), int(mode), ctypes.c_void_p(stream_handle))
+
+
+def call_bwd(name, ptrs, B, H, L, d, p, mode, stream_handle):
+    """Raw call of a backward entry point; ptrs = (q, k, v, dout, stats, dq,
+    dk, dv) integer device pointers.  Returns the status."""
+    return getattr(load_library(), name)(
+        *(ctypes.c_void_p(x) for x in ptrs), int(B), int(H), int(L), int(d), int(p), int(mode),
+        ctypes.c_void_p(stream_handle))
+
+
+def _check_like(q, *ts):
+    import torch
+    for t in ts:
+        if (not isinstance(t, torch.Tensor) or t.shape != q.shape or t.dtype != torch.bfloat16
+                or not t.is_contiguous() or t.device != q.device):
+            raise ValueError("tensors must be contiguous bfloat16 CUDA tensors shaped like q")
+
+
+def lssar_attn_fwd_train(q, k, v, p=3, mode=MODE_LSSAR, out=None, stats=None, stream=None):
+    """Training forward: returns (out, stats), stats [B, H, L, 4] float32 row
+    statistics {m, kappa, beta, W} for :func:`lssar_attn_bwd_simt`."""
+    import torch
+    if q.device.type != "cuda":
+        raise ValueError("q must be a CUDA tensor")
+    _check_like(q, q, k, v)
+    B, H, L, d = q.shape
+    out = torch.empty_like(q) if out is None else out
+    _check_like(q, out)
+    if stats is None:
+        stats = torch.empty((B, H, L, 4), dtype=torch.float32, device=q.device)
+    elif stats.shape != (B, H, L, 4) or stats.dtype != torch.float32 or not stats.is_contiguous():
+        raise ValueError("stats must be a contiguous float32 [B, H, L, 4] tensor")
+    with torch.cuda.device(q.device):
+        s = torch.cuda.current_stream(q.device) if stream is None else stream
+        _check(call_train(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), stats.data_ptr(),
+                          B, H, L, d, p, mode, s.cuda_stream))
+    return out, stats
+
+
+def _backward(name, q, k, v, dout, stats, p, mode, stream):
+    import torch
+    if q.device.type != "cuda":
+        raise ValueError("q must be a CUDA tensor")
+    _check_like(q, q, k, v, dout)
+    B, H, L, d = q.shape
+    if stats.shape != (B, H, L, 4) or stats.dtype != torch.float32 or not stats.is_contiguous():
+        raise ValueError("stats must be the float32 [B, H, L, 4] tensor of lssar_attn_fwd_train")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    with torch.cuda.device(q.device):
+        s = torch.cuda.current_stream(q.device) if stream is None else stream
+        ptrs = tuple(t.data_ptr() for t in (q, k, v, dout, stats, dq, dk, dv))
+        _check(call_bwd(name, ptrs, B, H, L, d, p, mode, s.cuda_stream))
+    return dq, dk, dv
+
+
+def lssar_attn_bwd_simt(q, k, v, dout, stats, p=3, mode=MODE_LSSAR, stream=None):
+    """Gradients (dq, dk, dv) of sum(dout * out) on the plain CUDA-core
+    backward (cross-check path), from the row statistics of
+    :func:`lssar_attn_fwd_train`."""
+    return _backward("lssar_attn_bwd_simt", q, k, v, dout, stats, p, mode, stream)
 
 
 def call_heads_p(q_ptr, k_ptr, v_ptr, out_ptr, B, H, L, d, p_per_head, mode, stream_handle):

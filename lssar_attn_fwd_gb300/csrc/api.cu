@@ -72,10 +72,11 @@ cudaError_t device_pool(cudaMemPool_t *out) {
 }
 
 int run_tc(const void *q, const void *k, const void *v, void *out, int B, int H, int L, int d,
-           int p, int mode, cudaStream_t stream, const lssar::Events &ev) {
+           int p, int mode, cudaStream_t stream, const lssar::Events &ev, float *stats = nullptr) {
     lssar::Problem pr;
     const int st = validate(q, k, v, out, B, H, L, d, p, mode, &pr);
     if (st != LSSAR_OK) return st;
+    pr.stats = stats;
     const size_t ws_bytes = lssar::tc_workspace_bytes(pr);
     void *ws = nullptr;
     if (ws_bytes) {
@@ -86,6 +87,31 @@ int run_tc(const void *q, const void *k, const void *v, void *out, int B, int H,
     const cudaError_t e = lssar::launch_tc(pr, ws, stream, ev);
     if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
     return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
+}
+
+// Checks of the backward's arguments (pure host).
+int validate_bwd(const void *q, const void *k, const void *v, const void *dout, const float *stats,
+                 void *dq, void *dk, void *dv, int B, int H, int L, int d, int p, int mode,
+                 lssar::BwdProblem *bp) {
+    if (!stats || !dq || !dk || !dv) return LSSAR_ERR_NULL;
+    lssar::Problem pr;
+    // the forward's checks cover q, k, v and dout (dout in the place of out)
+    const int st = validate(q, k, v, const_cast<void *>(dout), B, H, L, d, p, mode, &pr);
+    if (st != LSSAR_OK) return st;
+    for (const void *ptr : {static_cast<const void *>(stats), static_cast<const void *>(dq),
+                            static_cast<const void *>(dk), static_cast<const void *>(dv)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15u) return LSSAR_ERR_ALIGN;
+    const size_t bytes = (size_t)B * H * L * d * 2, sbytes = (size_t)B * H * L * 16;
+    const void *outs[3] = {dq, dk, dv};
+    for (int a = 0; a < 3; ++a) {
+        for (const void *in : {q, k, v, dout})
+            if (ranges_overlap(outs[a], bytes, in, bytes)) return LSSAR_ERR_ALIAS;
+        if (ranges_overlap(outs[a], bytes, stats, sbytes)) return LSSAR_ERR_ALIAS;
+        for (int b = a + 1; b < 3; ++b)
+            if (ranges_overlap(outs[a], bytes, outs[b], bytes)) return LSSAR_ERR_ALIAS;
+    }
+    *bp = lssar::BwdProblem{q, k, v, dout, stats, dq, dk, dv, B, H, L, d, pr.p, mode};
+    return LSSAR_OK;
 }
 
 }  // namespace
@@ -110,6 +136,34 @@ int lssar_attn_fwd_profiled(const void *q, const void *k, const void *v, void *o
     ev.main = ev_main;
     ev.end = ev_end;
     return run_tc(q, k, v, out, B, H, L, d, p, mode, stream, ev);
+}
+
+int lssar_attn_fwd_train(const void *q, const void *k, const void *v, void *out, float *stats,
+                         int B, int H, int L, int d, int p, int mode, cudaStream_t stream) {
+    if (!stats) return LSSAR_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(stats) & 15u) return LSSAR_ERR_ALIGN;
+    if (B >= 1 && H >= 1 && L >= 1 && (d == 64 || d == 128)) {
+        const size_t bytes = (size_t)B * H * L * d * 2, sbytes = (size_t)B * H * L * 16;
+        for (const void *t : {q, k, v, static_cast<const void *>(out)})
+            if (t && ranges_overlap(stats, sbytes, t, bytes)) return LSSAR_ERR_ALIAS;
+    }
+    return run_tc(q, k, v, out, B, H, L, d, p, mode, stream, lssar::Events(), stats);
+}
+
+int lssar_attn_bwd_simt(const void *q, const void *k, const void *v, const void *dout,
+                        const float *stats, void *dq, void *dk, void *dv, int B, int H, int L,
+                        int d, int p, int mode, cudaStream_t stream) {
+    lssar::BwdProblem bp;
+    const int st = validate_bwd(q, k, v, dout, stats, dq, dk, dv, B, H, L, d, p, mode, &bp);
+    if (st != LSSAR_OK) return st;
+    cudaMemPool_t pool;
+    if (device_pool(&pool) != cudaSuccess) return LSSAR_ERR_CUDA;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, lssar::bwd_simt_workspace_bytes(bp), pool, stream) != cudaSuccess)
+        return LSSAR_ERR_CUDA;
+    const cudaError_t e = lssar::launch_bwd_simt(bp, ws, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
 }
 
 int lssar_attn_fwd_heads_p(const void *q, const void *k, const void *v, void *out, int B, int H,
@@ -187,7 +241,7 @@ const char *lssar_status_string(int status) {
         case LSSAR_ERR_MODE: return "unknown mode";
         case LSSAR_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
         case LSSAR_ERR_CUDA: return "CUDA error";
-        case LSSAR_ERR_ALIAS: return "out overlaps q, k or v";
+        case LSSAR_ERR_ALIAS: return "an output overlaps an input or another output";
         case LSSAR_ERR_SCRATCH: return "problem needs more scratch than the fixed no-alloc array";
         default: return "unknown status";
     }

@@ -21,6 +21,7 @@ struct Problem {
     void *out;
     int B, H, L, d, p, mode;
     const int *p_head = nullptr;   // host array of H exponents, or null (one p for all heads)
+    float *stats = nullptr;        // [B, H, L, 4] row statistics for the backward pass, or null
 };
 
 // Host-side argument checks of the C ABI (no CUDA call); LSSAR_OK or a
@@ -43,6 +44,17 @@ struct Events {
 size_t tc_workspace_bytes(const Problem &pr);
 cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Events &ev = Events());
 
+// Backward pass: gradients of sum(dout * out) for q, k, v, from the forward's
+// per-row statistics {m, kappa, beta, W} (float4 per row).
+struct BwdProblem {
+    const void *q, *k, *v, *dout;
+    const float *stats;
+    void *dq, *dk, *dv;
+    int B, H, L, d, p, mode;
+};
+// Plain CUDA-core backward; ws holds bwd_simt_workspace_bytes(pr) bytes.
+size_t bwd_simt_workspace_bytes(const BwdProblem &pr);
+cudaError_t launch_bwd_simt(const BwdProblem &pr, void *ws, cudaStream_t stream);
 // Decode: one query row per head (position L) against a K/V cache of L rows.
 struct DecodeProblem {
     const void *q;   // [B, H, d]

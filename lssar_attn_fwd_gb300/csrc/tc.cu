@@ -170,6 +170,7 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
     prm.per_head = pr.p_head ? 1 : 0;
     for (int h = 0; h < tc::kMaxHeadsP; ++h) prm.p_head[h] = (pr.p_head && h < pr.H) ? pr.p_head[h] : pr.p;
     prm.out = static_cast<__nv_bfloat16 *>(pr.out);
+    prm.stats = reinterpret_cast<float4 *>(pr.stats);
     prm.counter = counter;
     cudaError_t e = error_word_ptr(&prm.err);
     if (e != cudaSuccess) return e;

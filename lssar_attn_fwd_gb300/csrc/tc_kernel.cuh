@@ -109,6 +109,7 @@ struct Params {
     int per_head;    // 1: head h uses p_head[h] (generic power path only)
     int p_head[kMaxHeadsP];
     __nv_bfloat16 *out;
+    float4 *stats;       // per-row {m, kappa, beta, W} for the backward pass, or null
     unsigned *err;       // device error word
     unsigned *counter;   // work counter, zero at launch
 };
@@ -236,6 +237,7 @@ struct RowConst {
     float kappa;   // LSSAR slope
     float beta;    // LSSAR offset
     float m;       // softmax: row maximum of z
+    bool uniform;  // re-weighted row read as all-zero (prefix mean)
 };
 
 // Scores of one 32-column chunk to z = a * s in place; on the diagonal tile
@@ -682,6 +684,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             rc.kappa = 0.f;
             rc.beta = 0.f;
             rc.m = 0.f;
+            rc.uniform = false;
             if constexpr (kTwoPass) {
                 float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 constexpr float kInit = MODE == kSigmoidRw ? INFINITY : -INFINITY;
@@ -749,6 +752,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     } else {
                         rc.kappa = 1.f;   // all-zero re-weighted row: (2^(z-m))^p ~= 1
                         rc.beta = 0.f;
+                        rc.uniform = true;
                     }
                 } else if constexpr (MODE == kSigmoidRw) {
                     const float s1 = bars->x_s1[w][0][t] + bars->x_s1[w][1][t];
@@ -762,6 +766,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     } else {
                         rc.kappa = 1.f / sgm;   // all-zero re-weighted row
                         rc.beta = 0.f;
+                        rc.uniform = true;
                     }
                 } else {
                     const float s1 = bars->x_s1[w][0][t] + bars->x_s1[w][1][t];
@@ -779,6 +784,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         // uniform prefix mean.
                         rc.kappa = 1.f / spm;
                         rc.beta = 0.f;
+                        rc.uniform = true;
                     }
                 }
             }
@@ -845,6 +851,25 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int c = 0; c < NC; ++c) ptx::reg_fence(o[c]);
             ptx::tc_fence_before();
             ptx::mbar_arrive(o_free);
+            if (row < prm.L && h == 0 && prm.stats != nullptr) {
+                // Row statistics for the backward pass: the weights are
+                // w = max(phi kappa + beta, 0)^p (p = 1, kappa = 1, beta = 0 in the
+                // modes without re-weighting) and W = sum_j w.  A uniform row is
+                // stored as kappa = 0, beta = 1, W = i: constant weights, so its
+                // scores receive no gradient.
+                float4 st;
+                st.x = rc.m;
+                if constexpr (is_reweight(MODE)) {
+                    st.y = rc.uniform ? 0.f : rc.kappa;
+                    st.z = rc.uniform ? 1.f : rc.beta;
+                    st.w = rc.uniform ? fi : s2;
+                } else {
+                    st.y = 1.f;
+                    st.z = 0.f;
+                    st.w = s2;
+                }
+                prm.stats[(size_t)bh * prm.L + row] = st;
+            }
             if (row < prm.L) {
                 const float inv = 1.f / s2;
                 uint4 *dst = reinterpret_cast<uint4 *>(prm.out + ((size_t)bh * prm.L + row) * D +

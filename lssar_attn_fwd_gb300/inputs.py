@@ -103,6 +103,14 @@ def make_qkv(B, H, L, d, seed=0, structure="iid"):
     raise ValueError(f"unknown structure {structure!r}")
 
 
+def make_dout(B, H, L, d, seed=0):
+    """Seeded upstream gradient of the output for the backward pass: float32
+    N(0, 1) rounded to bf16 (uint16 bits, [B, H, L, d]), drawn from its own
+    stream (seed, 1) so it never repeats q, k or v."""
+    rng = np.random.default_rng([seed, 1])
+    return f32_to_bf16_bits(rng.standard_normal((B, H, L, d), dtype=np.float32))
+
+
 def make_workload(name, seed=0):
     """q, k, v bf16 bit arrays for a named workload."""
     w = WORKLOADS[name]

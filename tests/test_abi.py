@@ -122,3 +122,46 @@ def test_decode_invalid_arguments(lib):
     assert call_raw(f, Q, K, V, OUT, 1, 2, 16, 64, 0, 3, 0) == -4
     assert call_raw(f, Q, K + 2, V, OUT, 1, 2, 16, 64, 3, 2, 0) == -6
     assert call_raw(f, Q, K, V, K + 64, 1, 2, 16, 64, 3, 2, 0) == -8   # out inside the key cache
+
+
+STATS, DQ, DK, DV, DOUT = 5 << 32, 6 << 32, 7 << 32, 8 << 32, 9 << 32
+
+
+def test_train_invalid_arguments(lib):
+    from lssar_attn_fwd_gb300.api import call_train
+    assert call_train(Q, K, V, OUT, 0, 1, 2, 16, 64, 3, 2, 0) == -1           # no stats
+    assert call_train(0, K, V, OUT, STATS, 1, 2, 16, 64, 3, 2, 0) == -1
+    assert call_train(Q, K, V, OUT, STATS + 4, 1, 2, 16, 64, 3, 2, 0) == -6   # stats alignment
+    assert call_train(Q, K, V, OUT, Q + 256, 1, 2, 16, 64, 3, 2, 0) == -8     # stats inside q
+    assert call_train(Q, K, V, OUT, STATS, 1, 2, 16, 64, 0, 2, 0) == -4
+    assert call_train(Q, K, V, OUT, STATS, 1, 2, 16, 80, 3, 2, 0) == -3
+    assert call_train(Q, K, V, OUT, STATS, 1, 2, 16, 64, 3, 6, 0) == -5
+
+
+BWD_NAMES = ["lssar_attn_bwd_simt"]
+
+
+@pytest.mark.parametrize("name", BWD_NAMES)
+def test_backward_invalid_arguments(lib, name):
+    from lssar_attn_fwd_gb300.api import call_bwd
+    good = [Q, K, V, DOUT, STATS, DQ, DK, DV]
+
+    def c(idx=None, val=None, B=1, H=2, L=16, d=64, p=3, mode=2):
+        ptrs = list(good)
+        if idx is not None:
+            ptrs[idx] = val
+        return call_bwd(name, ptrs, B, H, L, d, p, mode, 0)
+
+    for idx in range(8):
+        assert c(idx, 0) == -1, idx                  # every pointer is required
+    assert c(mode=5) == -5
+    assert c(L=0) == -2
+    assert c(d=32) == -3
+    assert c(p=0) == -4
+    assert c(3, DOUT + 2) == -6
+    assert c(4, STATS + 8) == -6
+    assert c(7, DV + 4) == -6
+    assert c(5, Q + 64) == -8                         # dq over q
+    assert c(6, DOUT) == -8                           # dk over dout
+    assert c(7, STATS) == -8                          # dv over the stats
+    assert c(6, DQ + 256) == -8                       # dk overlaps dq
