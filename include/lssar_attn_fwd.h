@@ -111,6 +111,22 @@ int lssar_attn_fwd_train(const void *q, const void *k, const void *v, void *out,
                          int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
 
 /*
+ * Backward pass on the tensor cores: gradients of sum(dout * out) with
+ * respect to q, k and v, from the row statistics of lssar_attn_fwd_train.
+ * Same operation, arguments, results and errors as lssar_attn_bwd_simt below.
+ * Two persistent tcgen05 kernels: a pass over each 128-query tile (dq, and the
+ * per-query terms D_i = dout_i . out_i and the re-weighting threshold's
+ * gradient) and a pass over each 128-key tile (dk, dv); scores use fp16
+ * normalised rows as in the forward, the gradient products fp16 (normalised
+ * modes) or bf16 (softmax modes) with fp32 accumulation.  Scratch:
+ * 256 + 4*B*H + 4*B*H*L*d (normalised modes) + 32*B*H*ceil(L/128)*128 +
+ * 8*B*H*L*d bytes from the library's stream-ordered pool.
+ */
+int lssar_attn_bwd(const void *q, const void *k, const void *v, const void *dout,
+                   const float *stats, void *dq, void *dk, void *dv,
+                   int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
+
+/*
  * Backward pass: gradients of sum(dout * out) with respect to q, k and v,
  * given the row statistics of the forward (lssar_attn_fwd_train with the same
  * q, k, v, B, H, L, d, p, mode).  Chain rule through the steps of Key designs

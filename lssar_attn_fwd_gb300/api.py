@@ -22,6 +22,7 @@ _EXPORTS = (
     "lssar_attn_fwd_heads_p",
     "lssar_attn_decode",
     "lssar_attn_fwd_train",
+    "lssar_attn_bwd",
     "lssar_attn_bwd_simt",
     "lssar_status_string",
     "lssar_device_error_word",
@@ -60,7 +61,7 @@ def load_library():
     lib.lssar_attn_fwd_heads_p.restype = ctypes.c_int
     lib.lssar_attn_fwd_train.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
     lib.lssar_attn_fwd_train.restype = ctypes.c_int
-    for name in ("lssar_attn_bwd_simt",):
+    for name in ("lssar_attn_bwd", "lssar_attn_bwd_simt"):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
         fn.restype = ctypes.c_int
@@ -194,6 +195,13 @@ def _backward(name, q, k, v, dout, stats, p, mode, stream):
         ptrs = tuple(t.data_ptr() for t in (q, k, v, dout, stats, dq, dk, dv))
         _check(call_bwd(name, ptrs, B, H, L, d, p, mode, s.cuda_stream))
     return dq, dk, dv
+
+
+def lssar_attn_bwd(q, k, v, dout, stats, p=3, mode=MODE_LSSAR, stream=None):
+    """Gradients (dq, dk, dv) of sum(dout * out) on the tensor-core backward,
+    from the row statistics of :func:`lssar_attn_fwd_train` (same q, k, v, p,
+    mode).  Runs asynchronously on ``stream`` (default: the current stream)."""
+    return _backward("lssar_attn_bwd", q, k, v, dout, stats, p, mode, stream)
 
 
 def lssar_attn_bwd_simt(q, k, v, dout, stats, p=3, mode=MODE_LSSAR, stream=None):

@@ -150,6 +150,22 @@ int lssar_attn_fwd_train(const void *q, const void *k, const void *v, void *out,
     return run_tc(q, k, v, out, B, H, L, d, p, mode, stream, lssar::Events(), stats);
 }
 
+int lssar_attn_bwd(const void *q, const void *k, const void *v, const void *dout, const float *stats,
+                   void *dq, void *dk, void *dv, int B, int H, int L, int d, int p, int mode,
+                   cudaStream_t stream) {
+    lssar::BwdProblem bp;
+    const int st = validate_bwd(q, k, v, dout, stats, dq, dk, dv, B, H, L, d, p, mode, &bp);
+    if (st != LSSAR_OK) return st;
+    cudaMemPool_t pool;
+    if (device_pool(&pool) != cudaSuccess) return LSSAR_ERR_CUDA;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, lssar::bwd_tc_workspace_bytes(bp), pool, stream) != cudaSuccess)
+        return LSSAR_ERR_CUDA;
+    const cudaError_t e = lssar::launch_bwd_tc(bp, ws, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
+}
+
 int lssar_attn_bwd_simt(const void *q, const void *k, const void *v, const void *dout,
                         const float *stats, void *dq, void *dk, void *dv, int B, int H, int L,
                         int d, int p, int mode, cudaStream_t stream) {

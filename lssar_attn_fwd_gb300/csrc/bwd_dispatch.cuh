@@ -1,0 +1,60 @@
+// Launch of the backward-kernel template instances, one translation unit per
+// head dimension (bwd_d64.cu, bwd_d128.cu) so that they compile in parallel.
+#pragma once
+
+#include "bwd_kernel.cuh"
+
+namespace lssar {
+namespace tcb {
+
+// The four tensor maps in the roles of the pass: anchor tiles X1 (score
+// operand) and X2 (bf16), streamed tiles Y1 (score operand) and Y2 (bf16).
+struct Maps {
+    CUtensorMap x1, x2, y1, y2;
+};
+
+cudaError_t dispatch_d64(const BwdProblem &pr, int pass, const Maps &m, const Params &prm, int grid,
+                         cudaStream_t s);
+cudaError_t dispatch_d128(const BwdProblem &pr, int pass, const Maps &m, const Params &prm, int grid,
+                          cudaStream_t s);
+
+template <int D, int MODE, int PK, int PASS>
+cudaError_t launch_kernel(const Maps &m, const Params &prm, int grid, cudaStream_t stream) {
+    auto kern = lssar_bwd_kernel<D, MODE, PK, PASS>;
+    constexpr int smem = Cfg<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, stream>>>(m.x1, m.x2, m.y1, m.y2, prm);
+    return cudaGetLastError();
+}
+
+// Re-weighting modes: fixed power chains for p = 3 and 15, square-and-multiply otherwise.
+template <int D, int MODE, int PASS>
+cudaError_t dispatch_p(const BwdProblem &pr, const Maps &m, const Params &prm, int grid, cudaStream_t s) {
+    switch (pr.p) {
+        case 3: return launch_kernel<D, MODE, 3, PASS>(m, prm, grid, s);
+        case 15: return launch_kernel<D, MODE, 15, PASS>(m, prm, grid, s);
+        default: return launch_kernel<D, MODE, 0, PASS>(m, prm, grid, s);
+    }
+}
+
+template <int D, int PASS>
+cudaError_t dispatch_mode(const BwdProblem &pr, const Maps &m, const Params &prm, int grid, cudaStream_t s) {
+    switch (pr.mode) {
+        case kSoftmax: return launch_kernel<D, kSoftmax, 0, PASS>(m, prm, grid, s);
+        case kLssa: return launch_kernel<D, kLssa, 0, PASS>(m, prm, grid, s);
+        case kLssar: return dispatch_p<D, kLssar, PASS>(pr, m, prm, grid, s);
+        case kSoftmaxRw: return dispatch_p<D, kSoftmaxRw, PASS>(pr, m, prm, grid, s);
+        default: return dispatch_p<D, kSigmoidRw, PASS>(pr, m, prm, grid, s);
+    }
+}
+
+template <int D>
+cudaError_t dispatch(const BwdProblem &pr, int pass, const Maps &m, const Params &prm, int grid,
+                     cudaStream_t s) {
+    return pass == kRowPass ? dispatch_mode<D, kRowPass>(pr, m, prm, grid, s)
+                            : dispatch_mode<D, kColPass>(pr, m, prm, grid, s);
+}
+
+}  // namespace tcb
+}  // namespace lssar

@@ -1,0 +1,742 @@
+// Tensor-core backward pass of causal LSSAR / LSSA / softmax attention for sm_103a.
+//
+// Gradients of sum(dout * out) (the notes on "Softplus Attention with
+// Re-weighting Boosts Length Extrapolation in Large Language Models" train
+// with this attention; the formulas are the chain rule through Key designs
+// 1-2 in the forward kernel's log2 units).  For query row i (1-based) and key
+// j <= i, with the forward's saved row constants {m, kappa, beta, W}:
+//   z_ij = a_i s_ij         s = qh_i . kh_j (fp16 normalised rows) or q_i . k_j (softmax)
+//   b_ij = phi(z_ij)        log2(1 + 2^z) | 2^(z - m_i) | 1/(1 + 2^-z)
+//   w_ij = max(b kappa_i + beta_i, 0)^p = u_ij * max(b kappa_i + beta_i, 0)
+//   P_ij = w_ij / W_i,   dP_ij = dout_i . v_j,   D_i = sum_j P_ij dP_ij
+//   F_i  = p kappa_i / W_i,   dS1_i = -(O_i / i) F_i sum_j (dP_ij - D_i) u_ij
+//   ds_ij = a_i phi'(z_ij) (F_i (dP_ij - D_i) u_ij + dS1_i)
+//   dqh_i = sum_j ds_ij kh_j,  dkh_j = sum_i ds_ij qh_i,  dv_j = sum_i P_ij dout_i
+// (without re-weighting: p = 1, kappa = 1, beta = 0, u = 1, dS1 = 0).
+//
+// Two launches of one kernel template:
+//   row pass (PASS = kRowPass), one item per 128-query tile, anchor = (qh, dout):
+//     pass 1 over the key tiles: S = Qh Kh^T, dP = dO V^T; per row D_i, the
+//     sum for dS1_i and the range of dP (which bounds |ds| for the fp16 scale
+//     r_i); pass 2: S, dP again, ds / r_i -> TMEM, dQh += (ds / r_i) Kh.
+//     Writes dqh (fp32), the per-query record used by the column pass, and the
+//     per-head maximum R of r_i.
+//   column pass (PASS = kColPass), one item per 128-key tile, anchor = (kh, v):
+//     one pass over the query tiles i >= j: S^T = Kh Qh^T, dP^T = V dO^T,
+//     P^T and ds^T / R -> TMEM, dV += P^T dO, dKh += (ds^T / R) Qh.  The
+//     query records arrive with each tile (bulk copy into the stage).
+// The same stage tile serves as the K-major B operand of a score product and
+// as the MN-major B operand of an accumulation (the 128B-swizzled TMA layout
+// is both); ds is rounded to the score operands' type (fp16 for the
+// normalised modes), scaled into [-1, 1] per row (row pass) or per head
+// (column pass) so that fp16 cannot overflow.
+//
+// Roles (576 threads): warp 0 TMA producer, warp 1 TMEM owner + single-thread
+// MMA issuer, warps 2-17 four math warpgroups; warpgroup g owns partner
+// columns [32g, 32g+32) of every tile, thread t owns anchor row t (TMEM lane).
+// TMEM: S [0,128), dP [128,256), Acc1 [256,256+D), Acc2 (column pass)
+// [256+D,256+2D), A operands (packed 16-bit pairs, 64 columns each) after
+// them; column pass at d = 128: the A operands overwrite the first half of
+// each warpgroup's S / dP columns.
+// Every mbarrier wait is bounded; on expiry the kernel records a code in the
+// device error word, raises an abort flag and all roles leave their loops.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "lssar_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace lssar {
+namespace tcb {
+
+constexpr int kBM = 128;                  // anchor rows of an item (TMEM lanes)
+constexpr int kBN = 128;                  // partner rows of a streamed tile
+constexpr int kThreads = 576;
+constexpr int kMathWarp0 = 2;
+constexpr int kMathThreads = 4 * kBM;
+constexpr int kItemQ = 4;
+constexpr uint32_t kItemConsumers = 1 + kMathThreads;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kSuspendNs = 1000000;
+
+enum Pass : int { kRowPass = 0, kColPass = 1 };
+
+// Error codes in the device error word (the forward kernel uses 1-11).
+enum : unsigned { kErrXFull = 21, kErrXEmpty, kErrRingFull, kErrRingEmpty, kErrSFull, kErrSFree,
+                  kErrAFull, kErrAFree, kErrAccFull, kErrAccFree, kErrItem, kErrRed };
+
+constexpr uint32_t kKmajorLbo = 16, kKmajorSbo = 1024;    // K-major tiles
+constexpr uint32_t kMnLbo = 16384, kMnSbo = 1024;         // the same tiles read MN-major
+
+struct Params {
+    int BH, L;
+    int n_tiles;               // ceil(L / 128)
+    int n_items;               // BH * n_tiles
+    float ln_d;
+    int p;                     // exponent (generic power path)
+    const float4 *stats;       // row pass: [BH][L] {m, kappa, beta, W}
+    float4 *rowc;              // [BH][n_tiles * 128][2] per-query record (row pass writes)
+    unsigned *rmax;            // [BH] max of r_i as float bits (zero before the row pass)
+    float *acc_out;            // row pass: dqh, column pass: dkh; [BH][L][D] fp32
+    __nv_bfloat16 *dv;         // column pass: dv [BH][L][D]
+    unsigned *err;             // device error word
+    unsigned *counter;         // work counter, zero at launch
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int kTB = kBN * D * 2;                    // one 128-row tile
+    static constexpr int kConstBytes = kBN * 32;               // 128 query records
+    static constexpr int kStageBytes = 2 * kTB + kConstBytes;  // partner tiles + records
+    static constexpr int kStages = D == 64 ? 4 : 2;
+    static constexpr int kRingOff = 2 * kTB;                   // after the two anchor tiles
+    static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
+    static constexpr int kBarBytes = 12288;
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
+};
+
+template <int D, int PASS>
+struct Tmem {
+    static constexpr bool kAlias = PASS == kColPass && D == 128;
+    static constexpr uint32_t kS = 0, kDP = 128, kAcc1 = 256, kAcc2 = 256 + D;
+    static constexpr uint32_t kA1 = kAlias ? 0u : (PASS == kRowPass ? 256u + D : 256u + 2 * D);
+    static constexpr uint32_t kA2 = kAlias ? 128u : kA1 + 64;
+};
+static_assert(Tmem<128, kRowPass>::kA1 + 64 <= 512 && Tmem<64, kColPass>::kA2 + 64 <= 512, "TMEM");
+
+struct __align__(8) Barriers {
+    uint64_t x_full, x_empty;
+    uint64_t ring_full[4], ring_empty[4];
+    uint64_t s_full, s_free, a_full, a_free, acc_full, acc_free;
+    uint64_t red;              // row pass: the four warpgroups' partials are in x_red
+    uint64_t item_full[kItemQ], item_empty[kItemQ];
+    int item_q[kItemQ];
+    uint32_t tmem_base;
+    int abort_flag;
+    float x_red[5][4][kBM];    // row pass: partial row sums of the four warpgroups
+};
+static_assert(sizeof(Barriers) <= 12288, "barrier block too large");
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Barriers *b, unsigned *err,
+                                         unsigned code) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+        if ((spin & 15u) == 0) {
+            if (*(volatile int *)&b->abort_flag) return false;
+            if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+                atomicCAS(err, 0u, code);
+                *(volatile int *)&b->abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// u = base^(p-1) (and w = u * base by the caller); p = 1 gives the ReLU's
+// derivative, 1 for base > 0.
+template <int PK>
+__device__ __forceinline__ float2 pow_pm1(float2 b, int p) {
+    if constexpr (PK == 3) {
+        return __fmul2_rn(b, b);
+    } else if constexpr (PK == 15) {
+        const float2 b2 = __fmul2_rn(b, b), b3 = __fmul2_rn(b2, b), b6 = __fmul2_rn(b3, b3);
+        const float2 b7 = __fmul2_rn(b6, b);
+        return __fmul2_rn(b7, b7);
+    } else {
+        if (p == 1) return make_float2(b.x > 0.f ? 1.f : 0.f, b.y > 0.f ? 1.f : 0.f);
+        float2 acc = make_float2(1.f, 1.f), r = b;
+        int e = p - 1;
+        while (e) {
+            if (e & 1) acc = __fmul2_rn(acc, r);
+            r = __fmul2_rn(r, r);
+            e >>= 1;
+        }
+        return acc;
+    }
+}
+
+// Per-element quantities of a pair of scores z (already scaled).
+struct Elem {
+    float2 u;       // base^(p-1) (1 without re-weighting)
+    float2 w;       // the weight
+    float2 slope;   // dphi/dz
+};
+
+// Two elements (one per lane of the float2), each with its own row constants.
+template <int MODE, int PK>
+__device__ __forceinline__ Elem element(float2 z, float2 m, float2 kappa, float2 beta, int p) {
+    constexpr float kLn2 = 0.6931471805599453f;
+    Elem r;
+    float2 b;
+    if constexpr (MODE == kSoftmax || MODE == kSoftmaxRw) {
+        const float2 e = __fadd2_rn(z, make_float2(-m.x, -m.y));
+        b = make_float2(ptx::ex2(e.x), ptx::ex2(e.y));
+        r.slope = __fmul2_rn(b, make_float2(kLn2, kLn2));
+    } else if constexpr (MODE == kSigmoidRw) {
+        const float2 e = __fadd2_rn(make_float2(ptx::ex2(-z.x), ptx::ex2(-z.y)), make_float2(1.f, 1.f));
+        b = make_float2(ptx::rcp(e.x), ptx::rcp(e.y));
+        const float2 omb = __fadd2_rn(make_float2(1.f, 1.f), make_float2(-b.x, -b.y));
+        r.slope = __fmul2_rn(__fmul2_rn(b, omb), make_float2(kLn2, kLn2));
+    } else {
+        // sp2(z) = log2(1 + 2^z); dsp2/dz = 2^(z - sp2(z)), the logistic function
+        const float2 e = __fadd2_rn(make_float2(ptx::ex2(z.x), ptx::ex2(z.y)), make_float2(1.f, 1.f));
+        b = make_float2(ptx::lg2(e.x), ptx::lg2(e.y));
+        const float2 d = __fadd2_rn(z, make_float2(-b.x, -b.y));
+        r.slope = make_float2(ptx::ex2(d.x), ptx::ex2(d.y));
+    }
+    if constexpr (is_reweight(MODE)) {
+        const float2 t = __ffma2_rn(b, kappa, beta);
+        const float2 base = make_float2(fmaxf(t.x, 0.f), fmaxf(t.y, 0.f));
+        r.u = pow_pm1<PK>(base, p);
+        r.w = __fmul2_rn(r.u, base);
+    } else {
+        r.u = make_float2(1.f, 1.f);
+        r.w = b;
+    }
+    return r;
+}
+
+template <int MODE>
+__device__ __forceinline__ uint32_t pack_ds(float lo, float hi) {
+    if constexpr (uses_normalised_qk(MODE))
+        return ptx::pack_f16x2(lo, hi);
+    else
+        return ptx::pack_bf16x2(lo, hi);
+}
+
+template <int D, int MODE, int PK, int PASS>
+__global__ void __launch_bounds__(kThreads, 1)
+lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant__ CUtensorMap tmX2,
+                 const __grid_constant__ CUtensorMap tmY1, const __grid_constant__ CUtensorMap tmY2,
+                 const Params prm) {
+    using C = Cfg<D>;
+    using T = Tmem<D, PASS>;
+    constexpr int NS = C::kStages;
+    constexpr int TB = C::kTB;
+    constexpr bool kRaw = !uses_normalised_qk(MODE);
+    constexpr bool kRow = PASS == kRowPass;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sX = smem;
+    uint8_t *ring = smem + C::kRingOff;
+    Barriers *bars = reinterpret_cast<Barriers *>(smem + C::kBarOff);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // S = X1 Y1^T (score operands' type), dP = X2 Y2^T (bf16), M = N = 128
+    constexpr uint32_t kIdescS = ptx::idesc_f16(kRaw, kBM, kBN, false, false);
+    constexpr uint32_t kIdescDP = ptx::idesc_f16(true, kBM, kBN, false, false);
+    // Acc1 += A1 Y1 (A1 from TMEM, Y1 MN-major), Acc2 += A2 Y2 (bf16)
+    constexpr uint32_t kIdescA1 = ptx::idesc_f16(kRaw, kBM, D, false, true);
+    constexpr uint32_t kIdescA2 = ptx::idesc_f16(true, kBM, D, false, true);
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bars->x_full), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars->x_empty), 1);
+        for (int s = 0; s < NS; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&bars->ring_full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->ring_empty[s]), 1);
+        }
+        ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars->s_free), kMathThreads);
+        ptx::mbar_init(ptx::smem_u32(&bars->a_full), kMathThreads);
+        ptx::mbar_init(ptx::smem_u32(&bars->a_free), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars->acc_full), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars->acc_free), kMathThreads);
+        ptx::mbar_init(ptx::smem_u32(&bars->red), kMathThreads);
+        for (int s = 0; s < kItemQ; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&bars->item_full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->item_empty[s]), kItemConsumers);
+        }
+        bars->abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    const int BH = prm.BH;
+    // item -> head, anchor tile, partner tiles [p0, p1); longest items first
+    auto decode = [&](int item, int &bh, int &at, int &p0, int &p1) {
+        bh = item % BH;
+        if (kRow) {
+            at = prm.n_tiles - 1 - item / BH;
+            p0 = 0;
+            p1 = at + 1;
+        } else {
+            at = item / BH;
+            p0 = at;
+            p1 = prm.n_tiles;
+        }
+    };
+    auto next_item = [&](uint32_t &qi, int &item) -> bool {
+        const uint32_t s = qi % kItemQ, use = qi / kItemQ;
+        ++qi;
+        if (!wait_bar(ptx::smem_u32(&bars->item_full[s]), use & 1, bars, prm.err, kErrItem))
+            return false;
+        item = *(volatile int *)&bars->item_q[s];
+        ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[s]));
+        return true;
+    };
+    constexpr int kPasses = kRow ? 2 : 1;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            ptx::prefetch_tensormap(&tmX1);
+            ptx::prefetch_tensormap(&tmX2);
+            ptx::prefetch_tensormap(&tmY1);
+            ptx::prefetch_tensormap(&tmY2);
+            uint32_t ring_idx = 0, x_cnt = 0, qi = 0;
+            bool ok = true;
+            while (ok) {
+                const uint32_t s = qi % kItemQ, use = qi / kItemQ;
+                const int item = qi == 0 ? (int)blockIdx.x
+                                         : (int)(gridDim.x + atomicAdd(prm.counter, 1u));
+                ++qi;
+                if (use > 0 && !wait_bar(ptx::smem_u32(&bars->item_empty[s]), (use - 1) & 1, bars,
+                                         prm.err, kErrItem))
+                    break;
+                *(volatile int *)&bars->item_q[s] = item;
+                ptx::mbar_arrive(ptx::smem_u32(&bars->item_full[s]));
+                if (item >= prm.n_items) break;
+                int bh, at, p0, p1;
+                decode(item, bh, at, p0, p1);
+                if (x_cnt > 0 && !wait_bar(ptx::smem_u32(&bars->x_empty), (x_cnt - 1) & 1, bars,
+                                           prm.err, kErrXEmpty))
+                    break;
+                const uint32_t xf = ptx::smem_u32(&bars->x_full);
+                ptx::mbar_arrive_expect_tx(xf, 2 * TB);
+#pragma unroll
+                for (int b = 0; b < D / 64; ++b) {
+                    ptx::tma_load_3d(ptx::smem_u32(sX + b * 16384), &tmX1, xf, b * 64, at * kBM, bh);
+                    ptx::tma_load_3d(ptx::smem_u32(sX + TB + b * 16384), &tmX2, xf, b * 64, at * kBM, bh);
+                }
+                ++x_cnt;
+                for (int pass = 0; ok && pass < kPasses; ++pass) {
+                    for (int t = p0; ok && t < p1; ++t) {
+                        const uint32_t st = ring_idx % NS, su = ring_idx / NS;
+                        if (su > 0 && !wait_bar(ptx::smem_u32(&bars->ring_empty[st]), (su - 1) & 1, bars,
+                                                prm.err, kErrRingEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *stage = ring + st * C::kStageBytes;
+                        const uint32_t full = ptx::smem_u32(&bars->ring_full[st]);
+                        ptx::mbar_arrive_expect_tx(full, 2 * TB + (kRow ? 0 : C::kConstBytes));
+#pragma unroll
+                        for (int b = 0; b < D / 64; ++b) {
+                            ptx::tma_load_3d(ptx::smem_u32(stage + b * 16384), &tmY1, full, b * 64,
+                                             t * kBN, bh);
+                            ptx::tma_load_3d(ptx::smem_u32(stage + TB + b * 16384), &tmY2, full, b * 64,
+                                             t * kBN, bh);
+                        }
+                        if (!kRow)
+                            ptx::bulk_load(ptx::smem_u32(stage + 2 * TB),
+                                           prm.rowc + ((size_t)bh * prm.n_tiles * kBN + (size_t)t * kBN) * 2,
+                                           C::kConstBytes, full);
+                        ++ring_idx;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t ring_idx = 0, x_cnt = 0, qi = 0;
+            uint32_t sf_phase = 0, af_phase = 0, accf_phase = 0;
+            bool s_pending = false, acc_pending = false;
+            bool ok = true;
+            auto acquire = [&](uint32_t &slot) -> bool {
+                slot = ring_idx % NS;
+                const uint32_t use = ring_idx / NS;
+                ++ring_idx;
+                if (!wait_bar(ptx::smem_u32(&bars->ring_full[slot]), use & 1, bars, prm.err, kErrRingFull))
+                    return false;
+                ptx::tc_fence_after();
+                return true;
+            };
+            auto touch_s = [&]() -> bool {
+                if (!s_pending) return true;
+                if (!wait_bar(ptx::smem_u32(&bars->s_free), sf_phase, bars, prm.err, kErrSFree))
+                    return false;
+                sf_phase ^= 1;
+                s_pending = false;
+                ptx::tc_fence_after();
+                return true;
+            };
+            const uint64_t dx1 = ptx::smem_desc_sw128(ptx::smem_u32(sX), kKmajorLbo, kKmajorSbo);
+            const uint64_t dx2 = ptx::smem_desc_sw128(ptx::smem_u32(sX + TB), kKmajorLbo, kKmajorSbo);
+            const uint64_t dy0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kKmajorLbo, kKmajorSbo);
+            const uint64_t dm0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kMnLbo, kMnSbo);
+            // S and dP of the partner tile in `slot`
+            auto issue_scores = [&](uint32_t slot) {
+                const uint64_t y1 = dy0 + (uint64_t)((slot * C::kStageBytes) >> 4);
+                const uint64_t y2 = dy0 + (uint64_t)((slot * C::kStageBytes + TB) >> 4);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = ((k / 4) * 16384 + (k % 4) * 32) >> 4;
+                    ptx::mma_ss(tmem + T::kS, dx1 + off, y1 + off, kIdescS, k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = ((k / 4) * 16384 + (k % 4) * 32) >> 4;
+                    ptx::mma_ss(tmem + T::kDP, dx2 + off, y2 + off, kIdescDP, k > 0);
+                }
+                ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+                // with the A operands over S / dP the warpgroups signal a_full only
+                s_pending = !T::kAlias;
+            };
+            // A operand words of partner columns 16k..16k+15
+            auto a_addr = [&](uint32_t base, int k) -> uint32_t {
+                return T::kAlias ? tmem + base + 32 * (k / 2) + 8 * (k % 2) : tmem + base + 8 * k;
+            };
+            auto issue_acc = [&](uint32_t slot, bool accumulate) {
+                const uint64_t m1 = dm0 + (uint64_t)((slot * C::kStageBytes) >> 4);
+                const uint64_t m2 = dm0 + (uint64_t)((slot * C::kStageBytes + TB) >> 4);
+#pragma unroll
+                for (int k = 0; k < kBN / 16; ++k)
+                    ptx::mma_ts(tmem + T::kAcc1, a_addr(T::kA1, k), m1 + (uint64_t)((k * 2048) >> 4),
+                                kIdescA1, (accumulate || k > 0) ? 1u : 0u);
+                if (!kRow) {
+#pragma unroll
+                    for (int k = 0; k < kBN / 16; ++k)
+                        ptx::mma_ts(tmem + T::kAcc2, a_addr(T::kA2, k), m2 + (uint64_t)((k * 2048) >> 4),
+                                    kIdescA2, (accumulate || k > 0) ? 1u : 0u);
+                }
+            };
+            int item;
+            while (ok && (ok = next_item(qi, item)) && item < prm.n_items) {
+                int bh, at, p0, p1;
+                decode(item, bh, at, p0, p1);
+                const int n = p1 - p0;
+                if (!(ok = wait_bar(ptx::smem_u32(&bars->x_full), x_cnt & 1, bars, prm.err, kErrXFull)))
+                    break;
+                ++x_cnt;
+                ptx::tc_fence_after();
+                uint32_t slot;
+                if (kRow) {
+                    // pass 1: scores only
+                    for (int t = 0; ok && t < n; ++t) {
+                        if (!(ok = acquire(slot)) || !(ok = touch_s())) break;
+                        issue_scores(slot);
+                        ptx::mma_commit(ptx::smem_u32(&bars->ring_empty[slot]));
+                    }
+                    if (!ok) break;
+                }
+                // accumulation pass
+                uint32_t cur;
+                if (!(ok = acquire(cur)) || !(ok = touch_s())) break;
+                issue_scores(cur);
+                for (int t = 0; ok && t < n; ++t) {
+                    const bool has_next = t + 1 < n;
+                    uint32_t nxt = 0;
+                    if (!T::kAlias && has_next) {
+                        // next scores as soon as the warpgroups have loaded these
+                        if (!(ok = acquire(nxt)) || !(ok = touch_s())) break;
+                        issue_scores(nxt);
+                    }
+                    if (!(ok = wait_bar(ptx::smem_u32(&bars->a_full), af_phase, bars, prm.err, kErrAFull)))
+                        break;
+                    af_phase ^= 1;
+                    ptx::tc_fence_after();
+                    if (t == 0 && acc_pending) {
+                        if (!(ok = wait_bar(ptx::smem_u32(&bars->acc_free), accf_phase, bars, prm.err,
+                                            kErrAccFree)))
+                            break;
+                        accf_phase ^= 1;
+                        acc_pending = false;
+                        ptx::tc_fence_after();
+                    }
+                    issue_acc(cur, t > 0);
+                    ptx::mma_commit(ptx::smem_u32(&bars->a_free));
+                    ptx::mma_commit(ptx::smem_u32(&bars->ring_empty[cur]));
+                    if (T::kAlias && has_next) {
+                        // A was written over S / dP: the next scores follow the
+                        // accumulation in issue order
+                        if (!(ok = acquire(nxt))) break;
+                        issue_scores(nxt);
+                    }
+                    cur = nxt;
+                }
+                if (!ok) break;
+                ptx::mma_commit(ptx::smem_u32(&bars->acc_full));
+                ptx::mma_commit(ptx::smem_u32(&bars->x_empty));
+                acc_pending = true;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ math warpgroups
+        const int g = (warp - kMathWarp0) >> 2;
+        const int t = (warp & 3) * 32 + lane;            // anchor row within the tile = TMEM lane
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t s_col = tmem + lane_addr + T::kS + 32 * g;
+        const uint32_t dp_col = tmem + lane_addr + T::kDP + 32 * g;
+        const uint32_t a1_col = tmem + lane_addr + (T::kAlias ? T::kS + 32 * g : T::kA1 + 16 * g);
+        const uint32_t a2_col = tmem + lane_addr + (T::kAlias ? T::kDP + 32 * g : T::kA2 + 16 * g);
+        const uint32_t acc1_col = tmem + lane_addr + T::kAcc1 + g * (D / 4);
+        const uint32_t acc2_col = tmem + lane_addr + T::kAcc2 + g * (D / 4);
+        const uint32_t s_full = ptx::smem_u32(&bars->s_full), s_free = ptx::smem_u32(&bars->s_free);
+        const uint32_t a_full = ptx::smem_u32(&bars->a_full), a_free = ptx::smem_u32(&bars->a_free);
+        uint32_t sf_phase = 0, af_phase = 0, accf_phase = 0, red_phase = 0, qi = 0, ring_idx = 0;
+        bool a_pending = false;
+        const float log2e = 1.4426950408889634f;
+        const int pe = is_reweight(MODE) ? prm.p : 1;
+        auto wait_warp = [&](uint32_t bar, uint32_t parity, unsigned code) -> bool {
+            const bool mine = wait_bar(bar, parity, bars, prm.err, code);
+            return __all_sync(0xffffffffu, mine);
+        };
+        // S and dP of this thread's 32 columns into registers
+        auto load_scores = [&](uint32_t (&rs)[32], uint32_t (&rd)[32]) -> bool {
+            if (!wait_warp(s_full, sf_phase, kErrSFull)) return false;
+            sf_phase ^= 1;
+            ptx::tc_fence_after();
+            ptx::tmem_ld32(s_col, rs);
+            ptx::tmem_ld32(dp_col, rd);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence(rs);
+            ptx::reg_fence(rd);
+            if (!T::kAlias) {
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(s_free);
+            }
+            return true;
+        };
+        // A operand words into TMEM, then signal the MMA thread
+        auto store_a = [&](const uint32_t (&w1)[16], const uint32_t (&w2)[16]) -> bool {
+            if (!T::kAlias && a_pending) {
+                if (!wait_warp(a_free, af_phase, kErrAFree)) return false;
+                af_phase ^= 1;
+                ptx::tc_fence_after();
+            }
+            ptx::tmem_st16(a1_col, w1);
+            if (!kRow) ptx::tmem_st16(a2_col, w2);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(a_full);
+            a_pending = true;
+            return true;
+        };
+        bool ok = true;
+        int item;
+        while (ok) {
+            ok = __all_sync(0xffffffffu, next_item(qi, item));
+            if (!ok || item >= prm.n_items) break;
+            int bh, at, p0, p1;
+            decode(item, bh, at, p0, p1);
+            const int arow = at * kBM + t;                // anchor row (query or key)
+            const bool valid = arow < prm.L;
+            if (kRow) {
+                // ---------------- row pass: query row arow, key tiles 0..at
+                float4 st = make_float4(0.f, 0.f, 0.f, 1.f);
+                if (valid) st = prm.stats[(size_t)bh * prm.L + arow];
+                const float fi = (float)(arow + 1);
+                const float a = !valid ? 0.f : (kRaw ? log2e * rsqrtf((float)D) : log2e * prm.ln_d * logf(fi));
+                const float F = (float)pe * st.y / st.w;
+                const float2 mm = make_float2(st.x, st.x), kk = make_float2(st.y, st.y), bb = make_float2(st.z, st.z);
+                float2 e_acc = make_float2(0.f, 0.f), du_acc = make_float2(0.f, 0.f), u_acc = make_float2(0.f, 0.f);
+                float dmax = -INFINITY, dmin = INFINITY;
+                for (int kt = p0; kt < p1; ++kt) {
+                    uint32_t rs[32], rd[32];
+                    if (!(ok = load_scores(rs, rd))) break;
+                    const bool diag = kt == at;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const float2 z = __fmul2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])),
+                                                    make_float2(a, a));
+                        const float2 dP = make_float2(__uint_as_float(rd[c]), __uint_as_float(rd[c + 1]));
+                        Elem el = element<MODE, PK>(z, mm, kk, bb, pe);
+                        const bool m0 = diag && (32 * g + c > t), m1 = diag && (32 * g + c + 1 > t);
+                        if (m0) { el.w.x = 0.f; el.u.x = 0.f; }
+                        if (m1) { el.w.y = 0.f; el.u.y = 0.f; }
+                        e_acc = __ffma2_rn(el.w, dP, e_acc);
+                        du_acc = __ffma2_rn(el.u, dP, du_acc);
+                        u_acc = __fadd2_rn(u_acc, el.u);
+                        dmax = fmaxf(dmax, fmaxf(m0 ? -INFINITY : dP.x, m1 ? -INFINITY : dP.y));
+                        dmin = fminf(dmin, fminf(m0 ? INFINITY : dP.x, m1 ? INFINITY : dP.y));
+                    }
+                }
+                if (!ok) break;
+                bars->x_red[0][g][t] = e_acc.x + e_acc.y;
+                bars->x_red[1][g][t] = du_acc.x + du_acc.y;
+                bars->x_red[2][g][t] = u_acc.x + u_acc.y;
+                bars->x_red[3][g][t] = dmax;
+                bars->x_red[4][g][t] = dmin;
+                ptx::mbar_arrive(ptx::smem_u32(&bars->red));
+                if (!(ok = wait_warp(ptx::smem_u32(&bars->red), red_phase, kErrRed))) break;
+                red_phase ^= 1;
+                float esum = 0.f, dusum = 0.f, usum = 0.f, mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    esum += bars->x_red[0][h][t];
+                    dusum += bars->x_red[1][h][t];
+                    usum += bars->x_red[2][h][t];
+                    mx = fmaxf(mx, bars->x_red[3][h][t]);
+                    mn = fminf(mn, bars->x_red[4][h][t]);
+                }
+                const float Di = esum / st.w;
+                const float o = (is_reweight(MODE) && arow >= 3) ? 1.f : 0.f;
+                const float dS1 = -(o / fi) * F * (dusum - Di * usum);
+                const float dev = fmaxf(mx - Di, Di - mn);
+                float r = a * (F * dev + fabsf(dS1));
+                if (!(r > 0.f) || !valid) r = 1.f;
+                const float Fp = a * F / r, dS1p = a * dS1 / r;
+                if (g == 0) {
+                    // the column pass's record of this query (zero past L: no contribution)
+                    float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f), r1 = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (valid) {
+                        r0 = make_float4(a, st.x, st.y, st.z);
+                        r1 = make_float4(1.f / st.w, a * F, Di, a * dS1);
+                        atomicMax(prm.rmax + bh, __float_as_uint(a * (F * dev + fabsf(dS1))));
+                    }
+                    float4 *rec = prm.rowc + ((size_t)bh * prm.n_tiles * kBN + arow) * 2;
+                    rec[0] = r0;
+                    rec[1] = r1;
+                }
+                // pass 2: ds / r into TMEM, dqh accumulates in Acc1
+                for (int kt = p0; kt < p1; ++kt) {
+                    uint32_t rs[32], rd[32];
+                    if (!(ok = load_scores(rs, rd))) break;
+                    const bool diag = kt == at;
+                    uint32_t w1[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const float2 z = __fmul2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])),
+                                                    make_float2(a, a));
+                        const float2 dP = make_float2(__uint_as_float(rd[c]), __uint_as_float(rd[c + 1]));
+                        const Elem el = element<MODE, PK>(z, mm, kk, bb, pe);
+                        const float2 dd = __fadd2_rn(dP, make_float2(-Di, -Di));
+                        const float2 gg = __ffma2_rn(__fmul2_rn(dd, el.u), make_float2(Fp, Fp), make_float2(dS1p, dS1p));
+                        float2 ds = __fmul2_rn(gg, el.slope);
+                        if (diag && (32 * g + c > t)) ds.x = 0.f;
+                        if (diag && (32 * g + c + 1 > t)) ds.y = 0.f;
+                        w1[c / 2] = pack_ds<MODE>(ds.x, ds.y);
+                    }
+                    if (!(ok = store_a(w1, w1))) break;
+                }
+                if (!ok) break;
+                // epilogue: dqh = r * Acc1, this warpgroup's D/4 columns
+                if (!(ok = wait_warp(ptx::smem_u32(&bars->acc_full), accf_phase, kErrAccFull))) break;
+                accf_phase ^= 1;
+                ptx::tc_fence_after();
+                uint32_t acc[D / 4];
+                if constexpr (D == 64) {
+                    ptx::tmem_ld16(acc1_col, acc);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence(acc);
+                } else {
+                    ptx::tmem_ld32(acc1_col, acc);
+                    ptx::tmem_ld_wait();
+                    ptx::reg_fence(acc);
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ptx::smem_u32(&bars->acc_free));
+                if (valid) {
+                    float4 *dst = reinterpret_cast<float4 *>(prm.acc_out + ((size_t)bh * prm.L + arow) * D + g * (D / 4));
+#pragma unroll
+                    for (int c = 0; c < D / 16; ++c)
+                        dst[c] = make_float4(__uint_as_float(acc[4 * c]) * r, __uint_as_float(acc[4 * c + 1]) * r,
+                                             __uint_as_float(acc[4 * c + 2]) * r, __uint_as_float(acc[4 * c + 3]) * r);
+                }
+            } else {
+                // ---------------- column pass: key row arow, query tiles at..n_tiles-1
+                const float R = __uint_as_float(prm.rmax[bh]);
+                const float invR = R > 0.f ? 1.f / R : 0.f;
+                for (int qt = p0; qt < p1; ++qt) {
+                    uint32_t rs[32], rd[32];
+                    if (!(ok = load_scores(rs, rd))) break;
+                    // this tile's query records (the stage's bulk copy has landed:
+                    // its mbarrier phase is complete once S was issued)
+                    const uint32_t slot = ring_idx % NS, use = ring_idx / NS;
+                    ++ring_idx;
+                    if (!(ok = wait_warp(ptx::smem_u32(&bars->ring_full[slot]), use & 1, kErrRingFull))) break;
+                    const float4 *rec = reinterpret_cast<const float4 *>(ring + slot * C::kStageBytes + 2 * TB) + 64 * g;
+                    const bool diag = qt == at;
+                    uint32_t w1[16], w2[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const float4 ra0 = rec[2 * c], rb0 = rec[2 * c + 1];
+                        const float4 ra1 = rec[2 * c + 2], rb1 = rec[2 * c + 3];
+                        // ra = {a, m, kappa, beta}, rb = {1/W, a F, D, a dS1}
+                        const float2 z = __fmul2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])),
+                                                    make_float2(ra0.x, ra1.x));
+                        const float2 dP = make_float2(__uint_as_float(rd[c]), __uint_as_float(rd[c + 1]));
+                        const Elem el = element<MODE, PK>(z, make_float2(ra0.y, ra1.y), make_float2(ra0.z, ra1.z),
+                                                          make_float2(ra0.w, ra1.w), pe);
+                        const float2 P = __fmul2_rn(el.w, make_float2(rb0.x, rb1.x));
+                        const float2 dd = __fadd2_rn(dP, make_float2(-rb0.z, -rb1.z));
+                        const float2 gg = __ffma2_rn(__fmul2_rn(dd, el.u), make_float2(rb0.y, rb1.y),
+                                                     make_float2(rb0.w, rb1.w));
+                        const float2 ds = __fmul2_rn(__fmul2_rn(gg, el.slope), make_float2(invR, invR));
+                        float P0 = P.x, P1 = P.y, ds0 = ds.x, ds1 = ds.y;
+                        if (diag && (32 * g + c < t)) { P0 = 0.f; ds0 = 0.f; }
+                        if (diag && (32 * g + c + 1 < t)) { P1 = 0.f; ds1 = 0.f; }
+                        w1[c / 2] = pack_ds<MODE>(ds0, ds1);
+                        w2[c / 2] = ptx::pack_bf16x2(P0, P1);
+                    }
+                    if (!(ok = store_a(w1, w2))) break;
+                }
+                if (!ok) break;
+                // epilogue: dkh = R * Acc1, dv = Acc2
+                if (!(ok = wait_warp(ptx::smem_u32(&bars->acc_full), accf_phase, kErrAccFull))) break;
+                accf_phase ^= 1;
+                ptx::tc_fence_after();
+                uint32_t acc[D / 4], acc2[D / 4];
+                if constexpr (D == 64) {
+                    ptx::tmem_ld16(acc1_col, acc);
+                    ptx::tmem_ld16(acc2_col, acc2);
+                } else {
+                    ptx::tmem_ld32(acc1_col, acc);
+                    ptx::tmem_ld32(acc2_col, acc2);
+                }
+                ptx::tmem_ld_wait();
+                ptx::reg_fence(acc);
+                ptx::reg_fence(acc2);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ptx::smem_u32(&bars->acc_free));
+                if (valid) {
+                    const size_t off = ((size_t)bh * prm.L + arow) * D + g * (D / 4);
+                    float4 *dst = reinterpret_cast<float4 *>(prm.acc_out + off);
+                    uint4 *dvd = reinterpret_cast<uint4 *>(prm.dv + off);
+#pragma unroll
+                    for (int c = 0; c < D / 16; ++c)
+                        dst[c] = make_float4(__uint_as_float(acc[4 * c]) * R, __uint_as_float(acc[4 * c + 1]) * R,
+                                             __uint_as_float(acc[4 * c + 2]) * R, __uint_as_float(acc[4 * c + 3]) * R);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        const uint32_t *q8 = &acc2[8 * c];
+                        uint4 u;
+                        u.x = ptx::pack_bf16x2(__uint_as_float(q8[0]), __uint_as_float(q8[1]));
+                        u.y = ptx::pack_bf16x2(__uint_as_float(q8[2]), __uint_as_float(q8[3]));
+                        u.z = ptx::pack_bf16x2(__uint_as_float(q8[4]), __uint_as_float(q8[5]));
+                        u.w = ptx::pack_bf16x2(__uint_as_float(q8[6]), __uint_as_float(q8[7]));
+                        dvd[c] = u;
+                    }
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace tcb
+}  // namespace lssar

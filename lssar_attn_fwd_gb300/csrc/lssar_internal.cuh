@@ -55,6 +55,10 @@ struct BwdProblem {
 // Plain CUDA-core backward; ws holds bwd_simt_workspace_bytes(pr) bytes.
 size_t bwd_simt_workspace_bytes(const BwdProblem &pr);
 cudaError_t launch_bwd_simt(const BwdProblem &pr, void *ws, cudaStream_t stream);
+// Tensor-core backward (row pass, column pass, normalisation gradient); ws
+// holds bwd_tc_workspace_bytes(pr) bytes, 256-byte aligned.
+size_t bwd_tc_workspace_bytes(const BwdProblem &pr);
+cudaError_t launch_bwd_tc(const BwdProblem &pr, void *ws, cudaStream_t stream);
 // Decode: one query row per head (position L) against a K/V cache of L rows.
 struct DecodeProblem {
     const void *q;   // [B, H, d]

@@ -8,6 +8,7 @@
 
 #include "tc_kernel.cuh"
 #include "tc_dispatch.cuh"
+#include "tc_host.cuh"
 
 namespace lssar {
 
@@ -60,6 +61,26 @@ __global__ void __launch_bounds__(256) normalize_rows_fp16(const __nv_bfloat16 *
     *reinterpret_cast<uint4 *>(dst) = u;
 }
 
+}  // namespace
+
+cudaError_t launch_normalize_fp16(const void *q, const void *k, void *qh, void *kh, long long rows,
+                                  int d, unsigned *counter, cudaStream_t stream) {
+    const long long threads = 2 * rows * (d / 8);
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const auto *qb = static_cast<const __nv_bfloat16 *>(q);
+    const auto *kb = static_cast<const __nv_bfloat16 *>(k);
+    auto *qo = static_cast<__half *>(qh);
+    auto *ko = static_cast<__half *>(kh);
+    if (d == 64)
+        normalize_rows_fp16<64><<<(unsigned)blocks, 256, 0, stream>>>(qb, kb, qo, ko, rows, counter);
+    else
+        normalize_rows_fp16<128><<<(unsigned)blocks, 256, 0, stream>>>(qb, kb, qo, ko, rows, counter);
+    return cudaGetLastError();
+}
+
+namespace {
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -73,6 +94,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     });
     return fn;
 }
+
+}  // namespace
 
 // [BH, L, D] tensor of 16-bit elements, boxes of 64 elements x 128 rows,
 // 128-byte swizzle; rows past L read as zero.
@@ -88,8 +111,10 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int BH, 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
 std::mutex g_sym_mutex;
 unsigned *g_err_ptr[64] = {};
+}  // namespace
 
 cudaError_t error_word_ptr(unsigned **out) {
     int dev = 0;
@@ -106,8 +131,6 @@ cudaError_t error_word_ptr(unsigned **out) {
     *out = g_err_ptr[dev];
     return cudaSuccess;
 }
-
-}  // namespace
 
 namespace {
 constexpr size_t kCounterBytes = 256;
@@ -138,16 +161,7 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
         const size_t half = qk_bytes(pr);
         __half *qh = reinterpret_cast<__half *>(static_cast<char *>(ws) + kCounterBytes);
         __half *kh = reinterpret_cast<__half *>(static_cast<char *>(ws) + kCounterBytes + half);
-        const long long threads = 2 * rows * (pr.d / 8);
-        const long long blocks = (threads + 255) / 256;
-        if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-        const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
-        const auto *k = static_cast<const __nv_bfloat16 *>(pr.k);
-        if (pr.d == 64)
-            normalize_rows_fp16<64><<<(unsigned)blocks, 256, 0, stream>>>(q, k, qh, kh, rows, counter);
-        else
-            normalize_rows_fp16<128><<<(unsigned)blocks, 256, 0, stream>>>(q, k, qh, kh, rows, counter);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_normalize_fp16(pr.q, pr.k, qh, kh, rows, pr.d, counter, stream);
         if (e != cudaSuccess) return e;
         qsrc = qh;
         ksrc = kh;

@@ -138,7 +138,7 @@ def test_train_invalid_arguments(lib):
     assert call_train(Q, K, V, OUT, STATS, 1, 2, 16, 64, 3, 6, 0) == -5
 
 
-BWD_NAMES = ["lssar_attn_bwd_simt"]
+BWD_NAMES = ["lssar_attn_bwd", "lssar_attn_bwd_simt"]
 
 
 @pytest.mark.parametrize("name", BWD_NAMES)
