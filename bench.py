@@ -397,6 +397,64 @@ def run_decode(args, mode, p):
         "gpu_launches": 3 * args.steps}), flush=True)
 
 
+def run_backward(args, wl, mode, p):
+    """Backward step: lssar_attn_bwd (row pass, column pass, normalisation
+    gradient) on the workload's q, k, v and a seeded upstream gradient, with
+    the row statistics of one lssar_attn_fwd_train call made before timing.
+    FLOPs: the five causal products of an attention backward (S recomputed,
+    dP = dO V^T, dV = P^T dO, dQ = dS K, dK = dS^T Q), 10 d per causal score
+    element; the kernels execute nine (the row pass streams the keys twice)."""
+    import torch
+    from lssar_attn_fwd_gb300 import api
+    from lssar_attn_fwd_gb300.build import build
+    from lssar_attn_fwd_gb300.inputs import make_dout
+    build()
+    api.load_library()
+    B, H, L, d = wl.B, wl.H, wl.L, wl.d
+    qb, kb, vb = make_qkv(*wl.shape, seed=0, structure=wl.structure)
+    db = make_dout(B, H, L, d, seed=0)
+    to_t = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    q, k, v, dout = (to_t(x) for x in (qb, kb, vb, db))
+    _, stats = api.lssar_attn_fwd_train(q, k, v, p=p, mode=mode)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        api.lssar_attn_bwd(q, k, v, dout, stats, p=p, mode=mode)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for a, b in ev:
+        flush.zero_()
+        a.record(s)
+        api.lssar_attn_bwd(q, k, v, dout, stats, p=p, mode=mode)
+        b.record(s)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
+    assert api.device_error_word() == 0
+    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    elems = B * H * L * (L + 1) / 2
+    tflops = 10 * d * elems / (ms * 1e-3) / 1e12
+    peak, kind = peaks()
+    mname = {v: k for k, v in MODE_NAMES.items()}[mode]
+    print(json.dumps({
+        "metric": "LSSAR causal bwd TFLOP/s (5 GEMMs: S, dP, dV, dQ, dK)", "value": tflops,
+        "unit": "TFLOP/s", "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "dtype": "fp16/bf16 operands, fp32 accumulate",
+        "config": {"workload": f"backward: {wl.name} B={B} H={H} L={L} d={d} mode={mname} p={p}",
+                   "l2": "flushed before every step (256 MiB write)"},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "peak_source": f"{kind} bf16_tflops (burst)"},
+        "clocks": sampler.summary(t0, t1),
+        "gpu_launches": (4 if uses_normalised(mode) else 3) * args.steps}), flush=True)
+
+
+def uses_normalised(mode):
+    return mode in (MODE_LSSA, MODE_LSSAR, MODE_SIGMOID_RW)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -409,6 +467,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", action="store_true", help="benchmark the decode step instead")
+    ap.add_argument("--backward", action="store_true", help="benchmark the backward pass instead")
     ap.add_argument("--decode-shape", type=int, nargs=4, default=[8, 12, 16384, 64],
                     metavar=("B", "H", "L", "D"))
     args = ap.parse_args()
@@ -422,6 +481,8 @@ def main():
         p = args.p
     if args.decode:
         run_decode(args, mode, p)
+    elif args.backward:
+        run_backward(args, wl, mode, p)
     elif args.impl == "reference":
         run_reference(args, wl, mode, p)
     else:

@@ -45,11 +45,16 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "lssar_internal.cuh"
 #include "tc_ptx.cuh"
 
 namespace lssar {
 namespace tcb {
+
+using Diag = std::true_type;       // the causal diagonal tile of an item
+using OffDiag = std::false_type;   // a tile without masked elements
 
 constexpr int kBM = 128;                  // anchor rows of an item (TMEM lanes)
 constexpr int kBN = 128;                  // partner rows of a streamed tile
@@ -77,7 +82,7 @@ struct Params {
     float ln_d;
     int p;                     // exponent (generic power path)
     const float4 *stats;       // row pass: [BH][L] {m, kappa, beta, W}
-    float4 *rowc;              // [BH][n_tiles * 128][2] per-query record (row pass writes)
+    float *rowc;               // [BH][n_tiles][8 fields][128] per-query records (row pass writes)
     unsigned *rmax;            // [BH] max of r_i as float bits (zero before the row pass)
     float *acc_out;            // row pass: dqh, column pass: dkh; [BH][L][D] fp32
     __nv_bfloat16 *dv;         // column pass: dv [BH][L][D]
@@ -134,6 +139,18 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Barriers
             }
         }
     }
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // u = base^(p-1) (and w = u * base by the caller); p = 1 gives the ReLU's
@@ -343,7 +360,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                         }
                         if (!kRow)
                             ptx::bulk_load(ptx::smem_u32(stage + 2 * TB),
-                                           prm.rowc + ((size_t)bh * prm.n_tiles * kBN + (size_t)t * kBN) * 2,
+                                           prm.rowc + ((size_t)bh * prm.n_tiles + t) * 8 * kBN,
                                            C::kConstBytes, full);
                         ++ring_idx;
                     }
@@ -548,25 +565,30 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 const float2 mm = make_float2(st.x, st.x), kk = make_float2(st.y, st.y), bb = make_float2(st.z, st.z);
                 float2 e_acc = make_float2(0.f, 0.f), du_acc = make_float2(0.f, 0.f), u_acc = make_float2(0.f, 0.f);
                 float dmax = -INFINITY, dmin = INFINITY;
-                for (int kt = p0; kt < p1; ++kt) {
-                    uint32_t rs[32], rd[32];
-                    if (!(ok = load_scores(rs, rd))) break;
-                    const bool diag = kt == at;
+                auto stats_tile = [&](const uint32_t (&rs)[32], const uint32_t (&rd)[32], auto diag) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
                         const float2 z = __fmul2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])),
                                                     make_float2(a, a));
-                        const float2 dP = make_float2(__uint_as_float(rd[c]), __uint_as_float(rd[c + 1]));
+                        float2 dP = make_float2(__uint_as_float(rd[c]), __uint_as_float(rd[c + 1]));
                         Elem el = element<MODE, PK>(z, mm, kk, bb, pe);
-                        const bool m0 = diag && (32 * g + c > t), m1 = diag && (32 * g + c + 1 > t);
-                        if (m0) { el.w.x = 0.f; el.u.x = 0.f; }
-                        if (m1) { el.w.y = 0.f; el.u.y = 0.f; }
+                        float2 lo = dP, hi = dP;
+                        if constexpr (decltype(diag)::value) {
+                            if (32 * g + c > t) { el.w.x = 0.f; el.u.x = 0.f; lo.x = INFINITY; hi.x = -INFINITY; }
+                            if (32 * g + c + 1 > t) { el.w.y = 0.f; el.u.y = 0.f; lo.y = INFINITY; hi.y = -INFINITY; }
+                        }
                         e_acc = __ffma2_rn(el.w, dP, e_acc);
                         du_acc = __ffma2_rn(el.u, dP, du_acc);
                         u_acc = __fadd2_rn(u_acc, el.u);
-                        dmax = fmaxf(dmax, fmaxf(m0 ? -INFINITY : dP.x, m1 ? -INFINITY : dP.y));
-                        dmin = fminf(dmin, fminf(m0 ? INFINITY : dP.x, m1 ? INFINITY : dP.y));
+                        dmax = max3(dmax, hi.x, hi.y);
+                        dmin = min3(dmin, lo.x, lo.y);
                     }
+                };
+                for (int kt = p0; kt < p1; ++kt) {
+                    uint32_t rs[32], rd[32];
+                    if (!(ok = load_scores(rs, rd))) break;
+                    if (kt == at) stats_tile(rs, rd, Diag());
+                    else stats_tile(rs, rd, OffDiag());
                 }
                 if (!ok) break;
                 bars->x_red[0][g][t] = e_acc.x + e_acc.y;
@@ -594,23 +616,17 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 if (!(r > 0.f) || !valid) r = 1.f;
                 const float Fp = a * F / r, dS1p = a * dS1 / r;
                 if (g == 0) {
-                    // the column pass's record of this query (zero past L: no contribution)
-                    float4 r0 = make_float4(0.f, 0.f, 0.f, 0.f), r1 = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (valid) {
-                        r0 = make_float4(a, st.x, st.y, st.z);
-                        r1 = make_float4(1.f / st.w, a * F, Di, a * dS1);
-                        atomicMax(prm.rmax + bh, __float_as_uint(a * (F * dev + fabsf(dS1))));
-                    }
-                    float4 *rec = prm.rowc + ((size_t)bh * prm.n_tiles * kBN + arow) * 2;
-                    rec[0] = r0;
-                    rec[1] = r1;
+                    // the column pass's record of this query, field-major per tile
+                    // (all zero past L: no contribution)
+                    const float fld[8] = {a, st.x, st.y, st.z, 1.f / st.w, a * F, Di, a * dS1};
+                    float *rec = prm.rowc + ((size_t)bh * prm.n_tiles + at) * 8 * kBN + t;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) rec[k * kBN] = valid ? fld[k] : 0.f;
+                    if (valid) atomicMax(prm.rmax + bh, __float_as_uint(a * (F * dev + fabsf(dS1))));
                 }
                 // pass 2: ds / r into TMEM, dqh accumulates in Acc1
-                for (int kt = p0; kt < p1; ++kt) {
-                    uint32_t rs[32], rd[32];
-                    if (!(ok = load_scores(rs, rd))) break;
-                    const bool diag = kt == at;
-                    uint32_t w1[16];
+                auto ds_tile = [&](const uint32_t (&rs)[32], const uint32_t (&rd)[32], uint32_t (&w1)[16],
+                                   auto diag) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
                         const float2 z = __fmul2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])),
@@ -620,10 +636,19 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                         const float2 dd = __fadd2_rn(dP, make_float2(-Di, -Di));
                         const float2 gg = __ffma2_rn(__fmul2_rn(dd, el.u), make_float2(Fp, Fp), make_float2(dS1p, dS1p));
                         float2 ds = __fmul2_rn(gg, el.slope);
-                        if (diag && (32 * g + c > t)) ds.x = 0.f;
-                        if (diag && (32 * g + c + 1 > t)) ds.y = 0.f;
+                        if constexpr (decltype(diag)::value) {
+                            if (32 * g + c > t) ds.x = 0.f;
+                            if (32 * g + c + 1 > t) ds.y = 0.f;
+                        }
                         w1[c / 2] = pack_ds<MODE>(ds.x, ds.y);
                     }
+                };
+                for (int kt = p0; kt < p1; ++kt) {
+                    uint32_t rs[32], rd[32];
+                    if (!(ok = load_scores(rs, rd))) break;
+                    uint32_t w1[16];
+                    if (kt == at) ds_tile(rs, rd, w1, Diag());
+                    else ds_tile(rs, rd, w1, OffDiag());
                     if (!(ok = store_a(w1, w1))) break;
                 }
                 if (!ok) break;
@@ -654,6 +679,43 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 // ---------------- column pass: key row arow, query tiles at..n_tiles-1
                 const float R = __uint_as_float(prm.rmax[bh]);
                 const float invR = R > 0.f ? 1.f / R : 0.f;
+                // rec: this tile's query records, field-major ([field][128 queries])
+                auto col_tile = [&](const uint32_t (&rs)[32], const uint32_t (&rd)[32], const float *rec,
+                                    uint32_t (&w1)[16], uint32_t (&w2)[16], auto diag) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const int q0 = 32 * g + c;
+                        float4 f[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (k != 1 || MODE == kSoftmax || MODE == kSoftmaxRw)
+                                f[k] = *reinterpret_cast<const float4 *>(rec + k * kBN + q0);
+                        // fields: 0 a, 1 m, 2 kappa, 3 beta, 4 1/W, 5 a F, 6 D, 7 a dS1
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            auto pick = [&](int k) {
+                                return h == 0 ? make_float2(f[k].x, f[k].y) : make_float2(f[k].z, f[k].w);
+                            };
+                            const int cc = c + 2 * h;
+                            const float2 z = __fmul2_rn(make_float2(__uint_as_float(rs[cc]), __uint_as_float(rs[cc + 1])),
+                                                        pick(0));
+                            const float2 dP = make_float2(__uint_as_float(rd[cc]), __uint_as_float(rd[cc + 1]));
+                            const float2 mcol = (MODE == kSoftmax || MODE == kSoftmaxRw) ? pick(1) : make_float2(0.f, 0.f);
+                            const Elem el = element<MODE, PK>(z, mcol, pick(2), pick(3), pe);
+                            float2 P = __fmul2_rn(el.w, pick(4));
+                            const float2 dcol = pick(6);
+                            const float2 dd = __fadd2_rn(dP, make_float2(-dcol.x, -dcol.y));
+                            const float2 gg = __ffma2_rn(__fmul2_rn(dd, el.u), pick(5), pick(7));
+                            float2 ds = __fmul2_rn(__fmul2_rn(gg, el.slope), make_float2(invR, invR));
+                            if constexpr (decltype(diag)::value) {
+                                if (q0 + 2 * h < t) { P.x = 0.f; ds.x = 0.f; }
+                                if (q0 + 2 * h + 1 < t) { P.y = 0.f; ds.y = 0.f; }
+                            }
+                            w1[cc / 2] = pack_ds<MODE>(ds.x, ds.y);
+                            w2[cc / 2] = ptx::pack_bf16x2(P.x, P.y);
+                        }
+                    }
+                };
                 for (int qt = p0; qt < p1; ++qt) {
                     uint32_t rs[32], rd[32];
                     if (!(ok = load_scores(rs, rd))) break;
@@ -662,30 +724,10 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                     const uint32_t slot = ring_idx % NS, use = ring_idx / NS;
                     ++ring_idx;
                     if (!(ok = wait_warp(ptx::smem_u32(&bars->ring_full[slot]), use & 1, kErrRingFull))) break;
-                    const float4 *rec = reinterpret_cast<const float4 *>(ring + slot * C::kStageBytes + 2 * TB) + 64 * g;
-                    const bool diag = qt == at;
+                    const float *rec = reinterpret_cast<const float *>(ring + slot * C::kStageBytes + 2 * TB);
                     uint32_t w1[16], w2[16];
-#pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const float4 ra0 = rec[2 * c], rb0 = rec[2 * c + 1];
-                        const float4 ra1 = rec[2 * c + 2], rb1 = rec[2 * c + 3];
-                        // ra = {a, m, kappa, beta}, rb = {1/W, a F, D, a dS1}
-                        const float2 z = __fmul2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])),
-                                                    make_float2(ra0.x, ra1.x));
-                        const float2 dP = make_float2(__uint_as_float(rd[c]), __uint_as_float(rd[c + 1]));
-                        const Elem el = element<MODE, PK>(z, make_float2(ra0.y, ra1.y), make_float2(ra0.z, ra1.z),
-                                                          make_float2(ra0.w, ra1.w), pe);
-                        const float2 P = __fmul2_rn(el.w, make_float2(rb0.x, rb1.x));
-                        const float2 dd = __fadd2_rn(dP, make_float2(-rb0.z, -rb1.z));
-                        const float2 gg = __ffma2_rn(__fmul2_rn(dd, el.u), make_float2(rb0.y, rb1.y),
-                                                     make_float2(rb0.w, rb1.w));
-                        const float2 ds = __fmul2_rn(__fmul2_rn(gg, el.slope), make_float2(invR, invR));
-                        float P0 = P.x, P1 = P.y, ds0 = ds.x, ds1 = ds.y;
-                        if (diag && (32 * g + c < t)) { P0 = 0.f; ds0 = 0.f; }
-                        if (diag && (32 * g + c + 1 < t)) { P1 = 0.f; ds1 = 0.f; }
-                        w1[c / 2] = pack_ds<MODE>(ds0, ds1);
-                        w2[c / 2] = ptx::pack_bf16x2(P0, P1);
-                    }
+                    if (qt == at) col_tile(rs, rd, rec, w1, w2, Diag());
+                    else col_tile(rs, rd, rec, w1, w2, OffDiag());
                     if (!(ok = store_a(w1, w2))) break;
                 }
                 if (!ok) break;

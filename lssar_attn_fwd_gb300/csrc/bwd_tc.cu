@@ -142,7 +142,7 @@ cudaError_t launch_bwd_tc(const BwdProblem &pr, void *ws, cudaStream_t stream) {
     prm.ln_d = logf((float)pr.d);
     prm.p = pr.p;
     prm.stats = reinterpret_cast<const float4 *>(pr.stats);
-    prm.rowc = reinterpret_cast<float4 *>(base + lay.rowc);
+    prm.rowc = reinterpret_cast<float *>(base + lay.rowc);
     prm.rmax = reinterpret_cast<unsigned *>(base + lay.rmax);
     prm.acc_out = reinterpret_cast<float *>(base + lay.dqh);
     prm.dv = nullptr;
