@@ -7,23 +7,69 @@
 //
 // The work is a pair of matrix-vector products per head and is bound by HBM:
 // every key and value row is read once.  Each head's L keys are split into
-// chunks so that B*H*chunks CTAs fill the GPU:
+// chunks so that B*H*chunks CTAs fill the GPU in one wave:
 //   dec_scores   z_j for the chunk (kept in a float scratch so that pass 2 does
 //                not read K again), chunk max and chunk sum of the normaliser
 //   dec_weights  combines the head's chunk statistics into the row constants,
 //                computes the chunk's weights and its partial sum_j w_j v_j, S2
 //   dec_combine  sums the partials of each head and divides
 // Scores use log2 units as in the prefill kernel: z = log2(e) * x.
+//
+// The K (V) rows of a chunk are contiguous, so a producer warp streams them
+// with bulk copies (cp.async.bulk, 8 KB per stage) into a 4-stage shared-memory
+// ring; eight consumer warps read the rows from shared memory.  The first
+// stages are requested before the CTA's prologue, so the copy engine runs
+// ahead of the arithmetic.  Every wait on the ring is bounded: after 2 s the
+// kernel records a code in the device error word and leaves its loop.
 #include <cuda_bf16.h>
 
 #include "lssar_internal.cuh"
+#include "tc_host.cuh"
+#include "tc_ptx.cuh"
 
 namespace lssar {
 namespace {
 
-constexpr int kDecThreads = 256;
-constexpr int kDecMaxPerThread = 16;   // keys per thread in a chunk (chunk <= 4096)
+constexpr int kDecWarps = 8;                    // consumer warps
+constexpr int kDecThreads = kDecWarps * 32;     // consumer threads
+constexpr int kDecBlock = kDecThreads + 32;     // + the producer warp
+constexpr int kDecMaxChunk = 4096;              // keys per chunk (scores / weights in smem)
+constexpr int kDecStages = 4;
+constexpr int kDecStageBytes = 8192;
+constexpr int kDecCtasPerSm = 4;
+constexpr uint64_t kDecWaitLimitNs = 2000000000ull;
+// device error word codes of the decode kernels
+enum : unsigned { kErrDecFull = 41, kErrDecEmpty, kErrDecDrain };
 
+// Dynamic shared memory of the two streaming kernels.
+struct alignas(16) DecSmem {
+    uint8_t ring[kDecStages][kDecStageBytes];
+    float row[kDecMaxChunk];           // scores (dec_scores) or weights (dec_weights)
+    float red[kDecWarps + 1];
+    uint64_t full[kDecStages], empty[kDecStages];
+    int abort_flag;
+};
+
+// Bounded wait on an mbarrier phase.  With honour_abort it also gives up as
+// soon as another role of the CTA has raised the abort flag.
+__device__ __forceinline__ bool dec_wait(uint32_t bar, uint32_t parity, DecSmem *sm, unsigned *err,
+                                         unsigned code, bool honour_abort) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (ptx::mbar_try_wait_sleep(bar, parity, 200000)) return true;
+        if ((spin & 15u) == 0) {
+            if (honour_abort && *(volatile int *)&sm->abort_flag) return false;
+            if (ptx::globaltimer_ns() - t0 > kDecWaitLimitNs) {
+                atomicCAS(err, 0u, code);
+                *(volatile int *)&sm->abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Sum or max over all kDecBlock threads (every thread must call it).
 __device__ __forceinline__ float block_reduce(float x, bool is_max, float *red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -35,7 +81,7 @@ __device__ __forceinline__ float block_reduce(float x, bool is_max, float *red) 
     if (lane == 0) red[warp] = x;
     __syncthreads();
     float r = is_max ? -INFINITY : 0.f;
-    for (int w = 0; w < kDecThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+    for (int w = 0; w < kDecWarps + 1; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
     return r;
 }
 
@@ -65,91 +111,163 @@ __device__ __forceinline__ float powi(float x, int p) {
     return r;
 }
 
+// The chunk's rows as a stream of stages of KT rows; stage it % kDecStages
+// holds row block `it`.  The producer warp's lane 0 calls issue(0), issue(1), ...
 template <int D>
-__global__ void __launch_bounds__(kDecThreads)
+struct Ring {
+    static constexpr int KT = kDecStageBytes / (2 * D);   // rows per stage (64 or 32)
+    DecSmem *sm;
+    const __nv_bfloat16 *src;   // first row of the chunk
+    int n;                      // rows in the chunk
+    unsigned *err;
+    __device__ int stages() const { return (n + KT - 1) / KT; }
+    __device__ bool issue(int it) const {
+        const int s = it % kDecStages, use = it / kDecStages;
+        if (use > 0 && !dec_wait(ptx::smem_u32(&sm->empty[s]), (use - 1) & 1, sm, err, kErrDecEmpty, true))
+            return false;
+        const int rows = min(KT, n - it * KT);
+        const uint32_t bytes = (uint32_t)rows * D * 2;
+        const uint32_t full = ptx::smem_u32(&sm->full[s]);
+        ptx::mbar_arrive_expect_tx(full, bytes);
+        ptx::bulk_load(ptx::smem_u32(sm->ring[s]), src + (size_t)it * KT * D, bytes, full);
+        return true;
+    }
+    // Issues row blocks [from, to) in order; returns the number issued in total
+    // (fewer than `to` only after a wait gave up).
+    __device__ int issue_upto(int from, int to) const {
+        int it = from;
+        while (it < to && issue(it)) ++it;
+        return it;
+    }
+    // Before the CTA exits: every issued copy has landed (bounded wait, also
+    // after an abort, so that no copy is in flight when the CTA ends).
+    __device__ void drain(int issued) const {
+        for (int it = max(0, issued - kDecStages); it < issued; ++it)
+            dec_wait(ptx::smem_u32(&sm->full[it % kDecStages]), (it / kDecStages) & 1, sm, err, kErrDecDrain,
+                     false);
+    }
+};
+
+__device__ __forceinline__ void init_ring(DecSmem *sm) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kDecStages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&sm->full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sm->empty[s]), kDecWarps);
+        }
+        sm->abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    __syncthreads();
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecBlock, kDecCtasPerSm)
 dec_scores(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k, int L,
-           int chunk, int mode, float *__restrict__ z_out, float2 *__restrict__ part) {
+           int chunk, int mode, float *__restrict__ z_out, float2 *__restrict__ part, unsigned *err) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    DecSmem *sm = reinterpret_cast<DecSmem *>(dsm);
     __shared__ float qs[D];
-    __shared__ float red[kDecThreads / 32];
     const int bh = blockIdx.y, c = blockIdx.x, nch = gridDim.x;
     const int j0 = c * chunk, j1 = min(L, j0 + chunk);
+    const int n = j1 - j0;
     const bool raw = !uses_normalised_qk(mode);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool producer = warp == kDecWarps;
+    const Ring<D> ring{sm, k + ((size_t)bh * L + j0) * D, n, err};
+    const int n_st = ring.stages();
+    init_ring(sm);
+    int issued = 0;
+    if (producer && lane == 0) issued = ring.issue_upto(0, min(n_st, kDecStages));
     // query row, L2-normalised for the LSSA family
     float qss = 0.f;
-    for (int t = threadIdx.x; t < D; t += kDecThreads) {
+    for (int t = threadIdx.x; t < D; t += kDecBlock) {
         const float x = __bfloat162float(q[(size_t)bh * D + t]);
         qs[t] = x;
         qss += x * x;
     }
-    qss = block_reduce(qss, false, red);
+    qss = block_reduce(qss, false, sm->red);
     const float log2e = 1.4426950408889634f;
     const float a = raw ? log2e * rsqrtf((float)D)
                         : log2e * logf((float)D) * logf((float)L) / fmaxf(sqrtf(qss), 1e-12f);
-    // scores: a warp load covers KPW keys (16 bytes per lane, D/8 lanes per key),
-    // kUnroll loads in flight per lane; the lanes of a key then add their parts
-    constexpr int kParts = D / 8, KPW = 32 / kParts, kWarps = kDecThreads / 32, kUnroll = 4;
-    __shared__ float zs[kDecMaxPerThread * kDecThreads];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane / kParts, col8 = lane % kParts;
-    const int n = j1 - j0;
-    float qv[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) qv[e] = qs[col8 * 8 + e];
-    const __nv_bfloat16 *kb = k + ((size_t)bh * L + j0) * D + col8 * 8;
     float m = -INFINITY;
-    // The loop index is the same for every lane of the warp (the lane's key
-    // offset `sub` is added inside), so the shuffles below are convergent.
-    for (int base = warp * KPW; base < n; base += kWarps * KPW * kUnroll) {
-        uint4 u[kUnroll];
-#pragma unroll
-        for (int r = 0; r < kUnroll; ++r) {
-            const int jj = base + r * kWarps * KPW + sub;
-            u[r] = jj < n ? __ldg(reinterpret_cast<const uint4 *>(kb + (size_t)jj * D))
-                          : make_uint4(0u, 0u, 0u, 0u);
+    if (producer) {
+        if (lane == 0) {
+            issued = ring.issue_upto(issued, n_st);
+            ring.drain(issued);
         }
+        __syncwarp();
+    } else {
+        // a warp load covers KPW rows (16 bytes per lane, D/8 lanes per row);
+        // warp w takes rows [2w KPW, 2(w+1) KPW) of each stage
+        constexpr int kParts = D / 8, KPW = 32 / kParts, KT = Ring<D>::KT;
+        static_assert(KT == kDecWarps * 2 * KPW, "two loads per warp and stage");
+        const int sub = lane / kParts, col8 = lane % kParts;
+        float qv[8];
 #pragma unroll
-        for (int r = 0; r < kUnroll; ++r) {
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u[r]);
-            float dot = 0.f, kss = 0.f;
+        for (int e = 0; e < 8; ++e) qv[e] = qs[col8 * 8 + e];
+        for (int it = 0; it < n_st; ++it) {   // warp-uniform: the shuffles are convergent
+            const int s = it % kDecStages;
+            if (!__all_sync(0xffffffffu, dec_wait(ptx::smem_u32(&sm->full[s]), (it / kDecStages) & 1, sm,
+                                                  err, kErrDecFull, true)))
+                break;
 #pragma unroll
-            for (int f = 0; f < 4; ++f) {
-                const float2 v2 = __bfloat1622float2(h[f]);
-                dot = fmaf(v2.x, qv[2 * f], dot);
-                dot = fmaf(v2.y, qv[2 * f + 1], dot);
-                kss = fmaf(v2.x, v2.x, kss);
-                kss = fmaf(v2.y, v2.y, kss);
-            }
+            for (int r = 0; r < 2; ++r) {
+                const int kl = (2 * warp + r) * KPW + sub;   // row within the stage
+                const int jj = it * KT + kl;                 // row within the chunk
+                uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                if (jj < n) u = *reinterpret_cast<const uint4 *>(sm->ring[s] + kl * D * 2 + col8 * 16);
+                const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+                float dot = 0.f, kss = 0.f;
 #pragma unroll
-            for (int o = kParts / 2; o > 0; o >>= 1) {
-                dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                kss += __shfl_xor_sync(0xffffffffu, kss, o);
+                for (int f = 0; f < 4; ++f) {
+                    const float2 v2 = __bfloat1622float2(h[f]);
+                    dot = fmaf(v2.x, qv[2 * f], dot);
+                    dot = fmaf(v2.y, qv[2 * f + 1], dot);
+                    kss = fmaf(v2.x, v2.x, kss);
+                    kss = fmaf(v2.y, v2.y, kss);
+                }
+#pragma unroll
+                for (int o = kParts / 2; o > 0; o >>= 1) {
+                    dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                    kss += __shfl_xor_sync(0xffffffffu, kss, o);
+                }
+                if (col8 == 0 && jj < n) {
+                    const float z = raw ? a * dot : a * dot / fmaxf(sqrtf(kss), 1e-12f);
+                    sm->row[jj] = z;
+                    z_out[(size_t)bh * L + j0 + jj] = z;
+                    m = fmaxf(m, z);
+                }
             }
-            const int jj = base + r * kWarps * KPW + sub;
-            if (col8 == 0 && jj < n) {
-                const float z = raw ? a * dot : a * dot / fmaxf(sqrtf(kss), 1e-12f);
-                zs[jj] = z;
-                z_out[(size_t)bh * L + j0 + jj] = z;
-                m = fmaxf(m, z);
-            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm->empty[s]));
         }
     }
-    m = block_reduce(m, true, red);   // its barriers also publish zs
-    float s = 0.f;
-    for (int jj = threadIdx.x; jj < n; jj += kDecThreads) s += phi(mode, zs[jj], m);
-    s = block_reduce(s, false, red);
-    if (threadIdx.x == 0) part[(size_t)bh * nch + c] = make_float2(m, s);
+    m = block_reduce(m, true, sm->red);   // its barriers also publish the scores
+    float sum = 0.f;
+    for (int jj = threadIdx.x; jj < n; jj += kDecBlock) sum += phi(mode, sm->row[jj], m);
+    sum = block_reduce(sum, false, sm->red);
+    if (threadIdx.x == 0) part[(size_t)bh * nch + c] = make_float2(m, sum);
 }
 
 template <int D>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecBlock, kDecCtasPerSm)
 dec_weights(const __nv_bfloat16 *__restrict__ v, int L, int chunk, int mode, int p,
             const float *__restrict__ z_in, const float2 *__restrict__ part,
-            float *__restrict__ opart /* [BH][nch][D+1] */) {
-    __shared__ float wsm[kDecMaxPerThread * kDecThreads];
-    __shared__ float accs[kDecThreads / 32][D];
-    __shared__ float red[kDecThreads / 32];
+            float *__restrict__ opart /* [BH][nch][D+1] */, unsigned *err) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    DecSmem *sm = reinterpret_cast<DecSmem *>(dsm);
+    __shared__ float accs[kDecWarps][D];
     const int bh = blockIdx.y, c = blockIdx.x, nch = gridDim.x;
     const int j0 = c * chunk, j1 = min(L, j0 + chunk);
+    const int n = j1 - j0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool producer = warp == kDecWarps;
+    const Ring<D> ring{sm, v + ((size_t)bh * L + j0) * D, n, err};
+    const int n_st = ring.stages();
+    init_ring(sm);
+    int issued = 0;
+    if (producer && lane == 0) issued = ring.issue_upto(0, min(n_st, kDecStages));
     // row statistics of the head from its chunks
     float m = -INFINITY;
     for (int u = 0; u < nch; ++u) m = fmaxf(m, part[(size_t)bh * nch + u].x);
@@ -172,65 +290,69 @@ dec_weights(const __nv_bfloat16 *__restrict__ v, int L, int chunk, int mode, int
             uniform = true;   // all-zero re-weighted row: uniform prefix mean
         }
     }
-    for (int jj = threadIdx.x; jj < j1 - j0; jj += kDecThreads) {
+    for (int jj = threadIdx.x; jj < n; jj += kDecBlock) {
         const float z = z_in[(size_t)bh * L + j0 + jj];
         float w;
         if (mode == kSoftmax) w = exp2f(z - m);
         else if (mode == kLssa) w = sp2_any(z);
         else w = uniform ? 1.f : powi(fmaxf(phi(mode, z, m) * kappa + beta, 0.f), p);
-        wsm[jj] = w;
+        sm->row[jj] = w;
     }
     __syncthreads();
-    // partial sum_j w_j v_j: a warp load covers KPW keys (16 bytes per lane,
-    // D/8 lanes per key); each lane keeps kUnroll loads in flight
-    constexpr int kParts = D / 8, KPW = 32 / kParts, kWarps = kDecThreads / 32, kUnroll = 4;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane / kParts, col8 = lane % kParts;
-    const int n = j1 - j0;
-    float acc[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    const __nv_bfloat16 *vb = v + ((size_t)bh * L + j0) * D + col8 * 8;
-    for (int base = warp * KPW; base < n; base += kWarps * KPW * kUnroll) {   // warp-uniform
-        uint4 u[kUnroll];
-        float w[kUnroll];
-#pragma unroll
-        for (int r = 0; r < kUnroll; ++r) {
-            const int jj = base + r * kWarps * KPW + sub;
-            if (jj < n) {
-                u[r] = __ldg(reinterpret_cast<const uint4 *>(vb + (size_t)jj * D));
-                w[r] = wsm[jj];
-            } else {
-                u[r] = make_uint4(0u, 0u, 0u, 0u);
-                w[r] = 0.f;
-            }
+    if (producer) {
+        if (lane == 0) {
+            issued = ring.issue_upto(issued, n_st);
+            ring.drain(issued);
         }
+        __syncwarp();
+    } else {
+        // partial sum_j w_j v_j: a warp load covers KPW rows (16 bytes per lane,
+        // D/8 lanes per row); warp w takes rows [2w KPW, 2(w+1) KPW) of each stage
+        constexpr int kParts = D / 8, KPW = 32 / kParts, KT = Ring<D>::KT;
+        const int sub = lane / kParts, col8 = lane % kParts;
+        float acc[8];
 #pragma unroll
-        for (int r = 0; r < kUnroll; ++r) {
-            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u[r]);
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int it = 0; it < n_st; ++it) {
+            const int s = it % kDecStages;
+            if (!__all_sync(0xffffffffu, dec_wait(ptx::smem_u32(&sm->full[s]), (it / kDecStages) & 1, sm,
+                                                  err, kErrDecFull, true)))
+                break;
 #pragma unroll
-            for (int f = 0; f < 4; ++f) {
-                const float2 v2 = __bfloat1622float2(h[f]);
-                acc[2 * f] = fmaf(w[r], v2.x, acc[2 * f]);
-                acc[2 * f + 1] = fmaf(w[r], v2.y, acc[2 * f + 1]);
+            for (int r = 0; r < 2; ++r) {
+                const int kl = (2 * warp + r) * KPW + sub;
+                const int jj = it * KT + kl;
+                if (jj < n) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(sm->ring[s] + kl * D * 2 + col8 * 16);
+                    const float w = sm->row[jj];
+                    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        const float2 v2 = __bfloat1622float2(h[f]);
+                        acc[2 * f] = fmaf(w, v2.x, acc[2 * f]);
+                        acc[2 * f + 1] = fmaf(w, v2.y, acc[2 * f + 1]);
+                    }
+                }
             }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm->empty[s]));
         }
+        // the KPW row groups of a warp hold the same columns: fold them
+#pragma unroll
+        for (int o = kParts; o < 32; o <<= 1)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+        if (sub == 0)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) accs[warp][col8 * 8 + e] = acc[e];
     }
-    // the KPW key groups of a warp hold the same columns: fold them
-#pragma unroll
-    for (int o = kParts; o < 32; o <<= 1)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
-    if (sub == 0)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) accs[warp][col8 * 8 + e] = acc[e];
     float s2 = 0.f;
-    for (int jj = threadIdx.x; jj < n; jj += kDecThreads) s2 += wsm[jj];
-    s2 = block_reduce(s2, false, red);   // also orders the accs writes before the reads below
+    for (int jj = threadIdx.x; jj < n; jj += kDecBlock) s2 += sm->row[jj];
+    s2 = block_reduce(s2, false, sm->red);   // also orders the accs writes before the reads below
     float *dst = opart + ((size_t)bh * nch + c) * (D + 1);
-    for (int t = threadIdx.x; t < D; t += kDecThreads) {
+    for (int t = threadIdx.x; t < D; t += kDecBlock) {
         float r = 0.f;
-        for (int w2 = 0; w2 < kWarps; ++w2) r += accs[w2][t];
+        for (int w2 = 0; w2 < kDecWarps; ++w2) r += accs[w2][t];
         dst[t] = r;
     }
     if (threadIdx.x == 0) dst[D] = s2;
@@ -249,17 +371,35 @@ dec_combine(const float *__restrict__ opart, int nch, __nv_bfloat16 *__restrict_
     out[(size_t)bh * D + t] = __float2bfloat16_rn(o / s);
 }
 
-// Chunk length: a multiple of the block size, at most 16 keys per thread,
-// and enough chunks for about four CTAs per SM.
+// Chunk length: a multiple of 64 rows (whole stages at both head dimensions),
+// at most kDecMaxChunk, and chunks for at most kDecCtasPerSm CTAs per SM (one
+// wave) whenever the heads allow it.
 int choose_chunk(int BH, int L, int sms) {
-    const long long want_ctas = 4LL * sms;
-    long long nch = (want_ctas + BH - 1) / BH;
+    const long long slots = (long long)kDecCtasPerSm * sms;
+    long long nch = slots / BH;
     if (nch < 1) nch = 1;
     long long chunk = (L + nch - 1) / nch;
-    chunk = ((chunk + kDecThreads - 1) / kDecThreads) * kDecThreads;
-    if (chunk > (long long)kDecMaxPerThread * kDecThreads) chunk = (long long)kDecMaxPerThread * kDecThreads;
-    if (chunk < kDecThreads) chunk = kDecThreads;
+    chunk = ((chunk + 63) / 64) * 64;
+    if (chunk > kDecMaxChunk) chunk = kDecMaxChunk;
     return (int)chunk;
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, float *z, float2 *part,
+                     float *opart, unsigned *err, cudaStream_t stream) {
+    const int smem = (int)sizeof(DecSmem);
+    cudaError_t e = cudaFuncSetAttribute(dec_scores<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dec_weights<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(nch, BH);
+    const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
+    const auto *k = static_cast<const __nv_bfloat16 *>(pr.k);
+    const auto *v = static_cast<const __nv_bfloat16 *>(pr.v);
+    dec_scores<D><<<grid, kDecBlock, smem, stream>>>(q, k, pr.L, chunk, pr.mode, z, part, err);
+    dec_weights<D><<<grid, kDecBlock, smem, stream>>>(v, pr.L, chunk, pr.mode, pr.p, z, part, opart, err);
+    dec_combine<D><<<BH, D, 0, stream>>>(opart, nch, static_cast<__nv_bfloat16 *>(pr.out));
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -278,6 +418,8 @@ cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    unsigned *err = nullptr;
+    if ((e = error_word_ptr(&err)) != cudaSuccess) return e;
     const int BH = pr.B * pr.H;
     const int chunk = choose_chunk(BH, pr.L, sms);
     const int nch = (pr.L + chunk - 1) / chunk;
@@ -287,21 +429,8 @@ cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream
     float2 *part = reinterpret_cast<float2 *>(base + zb);
     const size_t pb = ((size_t)BH * nch * 8 + 255) & ~(size_t)255;
     float *opart = reinterpret_cast<float *>(base + zb + pb);
-    const dim3 grid(nch, BH);
-    const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
-    const auto *k = static_cast<const __nv_bfloat16 *>(pr.k);
-    const auto *v = static_cast<const __nv_bfloat16 *>(pr.v);
-    auto *o = static_cast<__nv_bfloat16 *>(pr.out);
-    if (pr.d == 64) {
-        dec_scores<64><<<grid, kDecThreads, 0, stream>>>(q, k, pr.L, chunk, pr.mode, z, part);
-        dec_weights<64><<<grid, kDecThreads, 0, stream>>>(v, pr.L, chunk, pr.mode, pr.p, z, part, opart);
-        dec_combine<64><<<BH, 64, 0, stream>>>(opart, nch, o);
-    } else {
-        dec_scores<128><<<grid, kDecThreads, 0, stream>>>(q, k, pr.L, chunk, pr.mode, z, part);
-        dec_weights<128><<<grid, kDecThreads, 0, stream>>>(v, pr.L, chunk, pr.mode, pr.p, z, part, opart);
-        dec_combine<128><<<BH, 128, 0, stream>>>(opart, nch, o);
-    }
-    return cudaGetLastError();
+    return pr.d == 64 ? launch_d<64>(pr, BH, chunk, nch, z, part, opart, err, stream)
+                      : launch_d<128>(pr, BH, chunk, nch, z, part, opart, err, stream);
 }
 
 }  // namespace lssar
