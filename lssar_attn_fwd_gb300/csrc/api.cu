@@ -224,10 +224,8 @@ int lssar_attn_decode(const void *q, const void *k_cache, const void *v_cache, v
         ranges_overlap(out, row_bytes, v_cache, cache_bytes))
         return LSSAR_ERR_ALIAS;
     lssar::DecodeProblem pr{q, k_cache, v_cache, out, B, H, L, d, reweight ? p : 1, mode};
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return LSSAR_ERR_CUDA;
+    int sms = 0;
+    if (lssar::device_sms(&sms) != cudaSuccess) return LSSAR_ERR_CUDA;
     cudaMemPool_t pool;
     if (device_pool(&pool) != cudaSuccess) return LSSAR_ERR_CUDA;
     void *ws = nullptr;

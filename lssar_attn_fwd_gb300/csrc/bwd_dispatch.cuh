@@ -22,7 +22,10 @@ template <int D, int MODE, int PK, int PASS>
 cudaError_t launch_kernel(const Maps &m, const Params &prm, int grid, cudaStream_t stream) {
     auto kern = lssar_bwd_kernel<D, MODE, PK, PASS>;
     constexpr int smem = Cfg<D>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static PerDeviceOnce once;
+    cudaError_t e = per_device_once(once, nullptr, [&](int &) {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    });
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, stream>>>(m.x1, m.x2, m.y1, m.y2, prm);
     return cudaGetLastError();

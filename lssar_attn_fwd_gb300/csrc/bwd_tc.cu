@@ -148,9 +148,8 @@ cudaError_t launch_bwd_tc(const BwdProblem &pr, void *ws, cudaStream_t stream) {
     prm.dv = nullptr;
     prm.counter = counters;
     if ((e = error_word_ptr(&prm.err)) != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int sms = 0;
+    if ((e = device_sms(&sms)) != cudaSuccess) return e;
     const int grid = prm.n_items < sms ? prm.n_items : sms;
 
     // row pass: anchor (q, dout), streamed (k, v)

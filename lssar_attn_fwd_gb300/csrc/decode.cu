@@ -39,7 +39,7 @@ constexpr int kDecStageBytes = 8192;
 constexpr int kDecCtasPerSm = 4;
 constexpr uint64_t kDecWaitLimitNs = 2000000000ull;
 // device error word codes of the decode kernels
-enum : unsigned { kErrDecFull = 41, kErrDecEmpty, kErrDecDrain };
+enum : unsigned { kErrDecFull = 41, kErrDecEmpty, kErrDecDrain, kErrDecGrid };
 
 // Dynamic shared memory of the two streaming kernels.
 struct alignas(16) DecSmem {
@@ -85,18 +85,19 @@ __device__ __forceinline__ float block_reduce(float x, bool is_max, float *red) 
     return r;
 }
 
-// log2(1 + 2^z) without overflow for any z
+// log2(1 + 2^z) without overflow for any z (MUFU ex2 / lg2, as in the
+// prefill kernel)
 __device__ __forceinline__ float sp2_any(float z) {
-    return fmaxf(z, 0.f) + log2f(1.f + exp2f(-fabsf(z)));
+    return fmaxf(z, 0.f) + ptx::lg2(1.f + ptx::ex2(-fabsf(z)));
 }
 
 __device__ __forceinline__ float sigmoid2(float z) {   // 1 / (1 + 2^-z)
-    return 1.f / (1.f + exp2f(-z));
+    return ptx::rcp(1.f + ptx::ex2(-z));
 }
 
 // The normaliser value of a score (softmax modes: relative to the max m).
 __device__ __forceinline__ float phi(int mode, float z, float m) {
-    if (mode == kSoftmax || mode == kSoftmaxRw) return exp2f(z - m);
+    if (mode == kSoftmax || mode == kSoftmaxRw) return ptx::ex2(z - m);
     if (mode == kSigmoidRw) return sigmoid2(z);
     return sp2_any(z);
 }
@@ -111,8 +112,10 @@ __device__ __forceinline__ float powi(float x, int p) {
     return r;
 }
 
-// The chunk's rows as a stream of stages of KT rows; stage it % kDecStages
-// holds row block `it`.  The producer warp's lane 0 calls issue(0), issue(1), ...
+// The chunk's rows as a stream of stages of KT rows: row block `it` goes to
+// the ring's stage sequence number base + it (slot (base + it) % kDecStages),
+// so a second stream can follow a first one through the same ring.  The
+// producer warp's lane 0 calls issue(0), issue(1), ...
 template <int D>
 struct Ring {
     static constexpr int KT = kDecStageBytes / (2 * D);   // rows per stage (64 or 32)
@@ -120,9 +123,12 @@ struct Ring {
     const __nv_bfloat16 *src;   // first row of the chunk
     int n;                      // rows in the chunk
     unsigned *err;
+    int base = 0;               // stage sequence number of row block 0
     __device__ int stages() const { return (n + KT - 1) / KT; }
+    __device__ int slot(int it) const { return (base + it) % kDecStages; }
+    __device__ uint32_t parity(int it) const { return ((base + it) / kDecStages) & 1; }
     __device__ bool issue(int it) const {
-        const int s = it % kDecStages, use = it / kDecStages;
+        const int s = slot(it), use = (base + it) / kDecStages;
         if (use > 0 && !dec_wait(ptx::smem_u32(&sm->empty[s]), (use - 1) & 1, sm, err, kErrDecEmpty, true))
             return false;
         const int rows = min(KT, n - it * KT);
@@ -143,8 +149,7 @@ struct Ring {
     // after an abort, so that no copy is in flight when the CTA ends).
     __device__ void drain(int issued) const {
         for (int it = max(0, issued - kDecStages); it < issued; ++it)
-            dec_wait(ptx::smem_u32(&sm->full[it % kDecStages]), (it / kDecStages) & 1, sm, err, kErrDecDrain,
-                     false);
+            dec_wait(ptx::smem_u32(&sm->full[slot(it)]), parity(it), sm, err, kErrDecDrain, false);
     }
 };
 
@@ -159,6 +164,109 @@ __device__ __forceinline__ void init_ring(DecSmem *sm) {
         ptx::fence_proxy_async_smem();
     }
     __syncthreads();
+}
+
+// Consumer warps (warps 0..7): the chunk's scores z_j into sm->row (and into
+// z_out[j] when z_out is not null); returns this thread's running max of z.
+// A warp load covers KPW rows (16 bytes per lane, D/8 lanes per row); warp w
+// takes rows [2w KPW, 2(w+1) KPW) of each stage.  The loop index is
+// warp-uniform, so the shuffles are convergent.
+template <int D>
+__device__ float consume_scores(const Ring<D> &ring, const float *qs, float a, bool raw, float *z_out) {
+    constexpr int kParts = D / 8, KPW = 32 / kParts, KT = Ring<D>::KT;
+    static_assert(KT == kDecWarps * 2 * KPW, "two loads per warp and stage");
+    DecSmem *sm = ring.sm;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane / kParts, col8 = lane % kParts;
+    const int n = ring.n, n_st = ring.stages();
+    float2 qv2[4];
+#pragma unroll
+    for (int f = 0; f < 4; ++f) qv2[f] = make_float2(qs[col8 * 8 + 2 * f], qs[col8 * 8 + 2 * f + 1]);
+    float m = -INFINITY;
+    for (int it = 0; it < n_st; ++it) {
+        const int s = ring.slot(it);
+        if (!__all_sync(0xffffffffu, dec_wait(ptx::smem_u32(&sm->full[s]), ring.parity(it), sm, ring.err,
+                                              kErrDecFull, true)))
+            break;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int kl = (2 * warp + r) * KPW + sub;   // row within the stage
+            const int jj = it * KT + kl;                 // row within the chunk
+            uint4 u = make_uint4(0u, 0u, 0u, 0u);
+            if (jj < n) u = *reinterpret_cast<const uint4 *>(sm->ring[s] + kl * D * 2 + col8 * 16);
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+            float2 dot2 = make_float2(0.f, 0.f), kss2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+                const float2 v2 = __bfloat1622float2(h[f]);
+                dot2 = __ffma2_rn(v2, qv2[f], dot2);
+                kss2 = __ffma2_rn(v2, v2, kss2);
+            }
+            float dot = dot2.x + dot2.y, kss = kss2.x + kss2.y;
+#pragma unroll
+            for (int o = kParts / 2; o > 0; o >>= 1) {
+                dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                kss += __shfl_xor_sync(0xffffffffu, kss, o);
+            }
+            if (col8 == 0 && jj < n) {
+                // |k| clamped at 1e-12 as everywhere: 1/max(|k|, eps) = rsqrt(max(|k|^2, eps^2))
+                const float z = raw ? a * dot : a * dot * rsqrtf(fmaxf(kss, 1e-24f));
+                sm->row[jj] = z;
+                if (z_out) z_out[jj] = z;
+                m = fmaxf(m, z);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm->empty[s]));
+    }
+    return m;
+}
+
+// Consumer warps: sum_j w_j v_j over the chunk's value rows, weights in
+// sm->row; each warp's partial (D columns) goes to accs[warp].
+template <int D>
+__device__ void consume_pv(const Ring<D> &ring, float (*accs)[D]) {
+    constexpr int kParts = D / 8, KPW = 32 / kParts, KT = Ring<D>::KT;
+    DecSmem *sm = ring.sm;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane / kParts, col8 = lane % kParts;
+    const int n = ring.n, n_st = ring.stages();
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int it = 0; it < n_st; ++it) {
+        const int s = ring.slot(it);
+        if (!__all_sync(0xffffffffu, dec_wait(ptx::smem_u32(&sm->full[s]), ring.parity(it), sm, ring.err,
+                                              kErrDecFull, true)))
+            break;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int kl = (2 * warp + r) * KPW + sub;
+            const int jj = it * KT + kl;
+            if (jj < n) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(sm->ring[s] + kl * D * 2 + col8 * 16);
+                const float w = sm->row[jj];
+                const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    const float2 r2 = __ffma2_rn(__bfloat1622float2(h[f]), make_float2(w, w),
+                                                 make_float2(acc[2 * f], acc[2 * f + 1]));
+                    acc[2 * f] = r2.x;
+                    acc[2 * f + 1] = r2.y;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm->empty[s]));
+    }
+    // the KPW row groups of a warp hold the same columns: fold them
+#pragma unroll
+    for (int o = kParts; o < 32; o <<= 1)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+    if (sub == 0)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) accs[warp][col8 * 8 + e] = acc[e];
 }
 
 template <int D>
@@ -198,56 +306,50 @@ dec_scores(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict_
         }
         __syncwarp();
     } else {
-        // a warp load covers KPW rows (16 bytes per lane, D/8 lanes per row);
-        // warp w takes rows [2w KPW, 2(w+1) KPW) of each stage
-        constexpr int kParts = D / 8, KPW = 32 / kParts, KT = Ring<D>::KT;
-        static_assert(KT == kDecWarps * 2 * KPW, "two loads per warp and stage");
-        const int sub = lane / kParts, col8 = lane % kParts;
-        float qv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qv[e] = qs[col8 * 8 + e];
-        for (int it = 0; it < n_st; ++it) {   // warp-uniform: the shuffles are convergent
-            const int s = it % kDecStages;
-            if (!__all_sync(0xffffffffu, dec_wait(ptx::smem_u32(&sm->full[s]), (it / kDecStages) & 1, sm,
-                                                  err, kErrDecFull, true)))
-                break;
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int kl = (2 * warp + r) * KPW + sub;   // row within the stage
-                const int jj = it * KT + kl;                 // row within the chunk
-                uint4 u = make_uint4(0u, 0u, 0u, 0u);
-                if (jj < n) u = *reinterpret_cast<const uint4 *>(sm->ring[s] + kl * D * 2 + col8 * 16);
-                const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-                float dot = 0.f, kss = 0.f;
-#pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                    const float2 v2 = __bfloat1622float2(h[f]);
-                    dot = fmaf(v2.x, qv[2 * f], dot);
-                    dot = fmaf(v2.y, qv[2 * f + 1], dot);
-                    kss = fmaf(v2.x, v2.x, kss);
-                    kss = fmaf(v2.y, v2.y, kss);
-                }
-#pragma unroll
-                for (int o = kParts / 2; o > 0; o >>= 1) {
-                    dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                    kss += __shfl_xor_sync(0xffffffffu, kss, o);
-                }
-                if (col8 == 0 && jj < n) {
-                    const float z = raw ? a * dot : a * dot / fmaxf(sqrtf(kss), 1e-12f);
-                    sm->row[jj] = z;
-                    z_out[(size_t)bh * L + j0 + jj] = z;
-                    m = fmaxf(m, z);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm->empty[s]));
-        }
+        m = consume_scores<D>(ring, qs, a, raw, z_out + (size_t)bh * L + j0);
     }
     m = block_reduce(m, true, sm->red);   // its barriers also publish the scores
     float sum = 0.f;
     for (int jj = threadIdx.x; jj < n; jj += kDecBlock) sum += phi(mode, sm->row[jj], m);
     sum = block_reduce(sum, false, sm->red);
     if (threadIdx.x == 0) part[(size_t)bh * nch + c] = make_float2(m, sum);
+}
+
+// The head's row constants from its chunks' (max, sum of phi), then the
+// weights of this chunk's n scores z[] into w[] (w may be z: in place).
+// Every thread of the CTA takes part.
+__device__ void chunk_weights(const float2 *__restrict__ part_head, int nch, int L, int mode, int p,
+                              const float *z, float *w, int n) {
+    // read through L2: other CTAs of the same launch may have written them
+    float m = -INFINITY;
+    for (int u = 0; u < nch; ++u) m = fmaxf(m, __ldcg(part_head + u).x);
+    float s1 = 0.f;
+    for (int u = 0; u < nch; ++u) {
+        const float2 pu = __ldcg(part_head + u);
+        s1 += (mode == kSoftmax || mode == kSoftmaxRw) ? pu.y * exp2f(pu.x - m) : pu.y;
+    }
+    float kappa = 0.f, beta = 0.f;
+    bool uniform = false;
+    if (is_reweight(mode)) {
+        const float o = (L <= 3) ? 0.f : 1.f;
+        const float theta = o * s1 / (float)L;
+        const float top = phi(mode, m, m);   // the normaliser at the row maximum
+        const float den = top - theta;
+        if (den > 1e-4f * top + 1e-6f) {
+            kappa = 1.f / den;
+            beta = -theta * kappa;
+        } else {
+            uniform = true;   // all-zero re-weighted row: uniform prefix mean
+        }
+    }
+    for (int jj = threadIdx.x; jj < n; jj += kDecBlock) {
+        const float zj = z[jj];
+        float wj;
+        if (mode == kSoftmax) wj = exp2f(zj - m);
+        else if (mode == kLssa) wj = sp2_any(zj);
+        else wj = uniform ? 1.f : powi(fmaxf(phi(mode, zj, m) * kappa + beta, 0.f), p);
+        w[jj] = wj;
+    }
 }
 
 template <int D>
@@ -268,36 +370,7 @@ dec_weights(const __nv_bfloat16 *__restrict__ v, int L, int chunk, int mode, int
     init_ring(sm);
     int issued = 0;
     if (producer && lane == 0) issued = ring.issue_upto(0, min(n_st, kDecStages));
-    // row statistics of the head from its chunks
-    float m = -INFINITY;
-    for (int u = 0; u < nch; ++u) m = fmaxf(m, part[(size_t)bh * nch + u].x);
-    float s1 = 0.f;
-    for (int u = 0; u < nch; ++u) {
-        const float2 pu = part[(size_t)bh * nch + u];
-        s1 += (mode == kSoftmax || mode == kSoftmaxRw) ? pu.y * exp2f(pu.x - m) : pu.y;
-    }
-    float kappa = 0.f, beta = 0.f;
-    bool uniform = false;
-    if (is_reweight(mode)) {
-        const float o = (L <= 3) ? 0.f : 1.f;
-        const float theta = o * s1 / (float)L;
-        const float top = phi(mode, m, m);   // the normaliser at the row maximum
-        const float den = top - theta;
-        if (den > 1e-4f * top + 1e-6f) {
-            kappa = 1.f / den;
-            beta = -theta * kappa;
-        } else {
-            uniform = true;   // all-zero re-weighted row: uniform prefix mean
-        }
-    }
-    for (int jj = threadIdx.x; jj < n; jj += kDecBlock) {
-        const float z = z_in[(size_t)bh * L + j0 + jj];
-        float w;
-        if (mode == kSoftmax) w = exp2f(z - m);
-        else if (mode == kLssa) w = sp2_any(z);
-        else w = uniform ? 1.f : powi(fmaxf(phi(mode, z, m) * kappa + beta, 0.f), p);
-        sm->row[jj] = w;
-    }
+    chunk_weights(part + (size_t)bh * nch, nch, L, mode, p, z_in + (size_t)bh * L + j0, sm->row, n);
     __syncthreads();
     if (producer) {
         if (lane == 0) {
@@ -306,45 +379,7 @@ dec_weights(const __nv_bfloat16 *__restrict__ v, int L, int chunk, int mode, int
         }
         __syncwarp();
     } else {
-        // partial sum_j w_j v_j: a warp load covers KPW rows (16 bytes per lane,
-        // D/8 lanes per row); warp w takes rows [2w KPW, 2(w+1) KPW) of each stage
-        constexpr int kParts = D / 8, KPW = 32 / kParts, KT = Ring<D>::KT;
-        const int sub = lane / kParts, col8 = lane % kParts;
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int it = 0; it < n_st; ++it) {
-            const int s = it % kDecStages;
-            if (!__all_sync(0xffffffffu, dec_wait(ptx::smem_u32(&sm->full[s]), (it / kDecStages) & 1, sm,
-                                                  err, kErrDecFull, true)))
-                break;
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int kl = (2 * warp + r) * KPW + sub;
-                const int jj = it * KT + kl;
-                if (jj < n) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(sm->ring[s] + kl * D * 2 + col8 * 16);
-                    const float w = sm->row[jj];
-                    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-                    for (int f = 0; f < 4; ++f) {
-                        const float2 v2 = __bfloat1622float2(h[f]);
-                        acc[2 * f] = fmaf(w, v2.x, acc[2 * f]);
-                        acc[2 * f + 1] = fmaf(w, v2.y, acc[2 * f + 1]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm->empty[s]));
-        }
-        // the KPW row groups of a warp hold the same columns: fold them
-#pragma unroll
-        for (int o = kParts; o < 32; o <<= 1)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
-        if (sub == 0)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) accs[warp][col8 * 8 + e] = acc[e];
+        consume_pv<D>(ring, accs);
     }
     float s2 = 0.f;
     for (int jj = threadIdx.x; jj < n; jj += kDecBlock) s2 += sm->row[jj];
@@ -371,6 +406,127 @@ dec_combine(const float *__restrict__ opart, int nch, __nv_bfloat16 *__restrict_
     out[(size_t)bh * D + t] = __float2bfloat16_rn(o / s);
 }
 
+// The whole decode step in one cooperative launch (every CTA resident):
+// phase A streams the chunk's keys (scores stay in shared memory) and
+// publishes the chunk's (max, sum of phi); the producer then already fetches
+// the first value stages into the same ring while the CTAs meet at a grid
+// barrier (bounded spin on a counter); phase B forms the weights from the
+// head's statistics and streams the values; the last CTA of each head to
+// finish (a per-head counter) sums the head's partials into the output.
+// sync: [0] grid barrier, [1 + bh] per-head counters, zero at launch.
+template <int D>
+__global__ void __launch_bounds__(kDecBlock, kDecCtasPerSm)
+dec_fused(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+          const __nv_bfloat16 *__restrict__ v, int L, int chunk, int mode, int p,
+          float2 *__restrict__ part, float *__restrict__ opart, __nv_bfloat16 *__restrict__ out,
+          unsigned *__restrict__ sync, unsigned *err) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    DecSmem *sm = reinterpret_cast<DecSmem *>(dsm);
+    __shared__ float qs[D];
+    __shared__ float accs[kDecWarps][D];
+    __shared__ int last_of_head;
+    const int bh = blockIdx.y, c = blockIdx.x, nch = gridDim.x;
+    const int j0 = c * chunk, j1 = min(L, j0 + chunk);
+    const int n = j1 - j0;
+    const bool raw = !uses_normalised_qk(mode);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool producer = warp == kDecWarps;
+    const Ring<D> rk{sm, k + ((size_t)bh * L + j0) * D, n, err, 0};
+    const int n_st = rk.stages();
+    const Ring<D> rv{sm, v + ((size_t)bh * L + j0) * D, n, err, n_st};
+    init_ring(sm);
+    int issued_k = 0, issued_v = 0;
+    if (producer && lane == 0) issued_k = rk.issue_upto(0, min(n_st, kDecStages));
+    // phase A: scores
+    float qss = 0.f;
+    for (int t = threadIdx.x; t < D; t += kDecBlock) {
+        const float x = __bfloat162float(q[(size_t)bh * D + t]);
+        qs[t] = x;
+        qss += x * x;
+    }
+    qss = block_reduce(qss, false, sm->red);
+    const float log2e = 1.4426950408889634f;
+    const float a = raw ? log2e * rsqrtf((float)D)
+                        : log2e * logf((float)D) * logf((float)L) / fmaxf(sqrtf(qss), 1e-12f);
+    float m = -INFINITY;
+    if (producer) {
+        if (lane == 0) {
+            issued_k = rk.issue_upto(issued_k, n_st);
+            // the first value stages follow as the consumers free the ring
+            if (issued_k == n_st) issued_v = rv.issue_upto(0, min(n_st, kDecStages));
+        }
+        __syncwarp();
+    } else {
+        m = consume_scores<D>(rk, qs, a, raw, nullptr);
+    }
+    m = block_reduce(m, true, sm->red);   // its barriers also publish the scores
+    float sum = 0.f;
+    for (int jj = threadIdx.x; jj < n; jj += kDecBlock) sum += phi(mode, sm->row[jj], m);
+    sum = block_reduce(sum, false, sm->red);
+    // grid barrier: every chunk's statistics are in `part`
+    if (threadIdx.x == 0) {
+        part[(size_t)bh * nch + c] = make_float2(m, sum);
+        __threadfence();
+        atomicAdd(sync, 1u);
+        const unsigned total = gridDim.x * gridDim.y;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (*(volatile unsigned *)sync < total) {
+            __nanosleep(256);
+            if (ptx::globaltimer_ns() - t0 > kDecWaitLimitNs) {
+                atomicCAS(err, 0u, (unsigned)kErrDecGrid);
+                *(volatile int *)&sm->abort_flag = 1;
+                break;
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    // phase B: weights in place of the scores, then the values
+    chunk_weights(part + (size_t)bh * nch, nch, L, mode, p, sm->row, sm->row, n);
+    __syncthreads();
+    if (producer) {
+        if (lane == 0) {
+            if (issued_k == n_st) issued_v = rv.issue_upto(issued_v, n_st);
+            // the last kDecStages copies of the K-then-V sequence have landed
+            // (earlier ones were consumed, and their slots reused)
+            const int total = issued_k + issued_v;
+            for (int g = max(0, total - kDecStages); g < total; ++g)
+                dec_wait(ptx::smem_u32(&sm->full[g % kDecStages]), (g / kDecStages) & 1, sm, err, kErrDecDrain,
+                         false);
+        }
+        __syncwarp();
+    } else {
+        consume_pv<D>(rv, accs);
+    }
+    float s2 = 0.f;
+    for (int jj = threadIdx.x; jj < n; jj += kDecBlock) s2 += sm->row[jj];
+    s2 = block_reduce(s2, false, sm->red);   // also orders the accs writes before the reads below
+    float *dst = opart + ((size_t)bh * nch + c) * (D + 1);
+    for (int t = threadIdx.x; t < D; t += kDecBlock) {
+        float r = 0.f;
+        for (int w2 = 0; w2 < kDecWarps; ++w2) r += accs[w2][t];
+        dst[t] = r;
+    }
+    if (threadIdx.x == 0) dst[D] = s2;
+    // the last chunk of the head to finish writes the head's output row
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last_of_head = atomicAdd(sync + 1 + bh, 1u) == (unsigned)(nch - 1);
+    __syncthreads();
+    if (last_of_head) {
+        __threadfence();
+        for (int t = threadIdx.x; t < D; t += kDecBlock) {
+            float o = 0.f, sw = 0.f;
+            for (int u = 0; u < nch; ++u) {
+                const volatile float *src = opart + ((size_t)bh * nch + u) * (D + 1);
+                o += src[t];
+                sw += src[D];
+            }
+            out[(size_t)bh * D + t] = __float2bfloat16_rn(o / sw);
+        }
+    }
+}
+
 // Chunk length: a multiple of 64 rows (whole stages at both head dimensions),
 // at most kDecMaxChunk, and chunks for at most kDecCtasPerSm CTAs per SM (one
 // wave) whenever the heads allow it.
@@ -384,14 +540,33 @@ int choose_chunk(int BH, int L, int sms) {
     return (int)chunk;
 }
 
+// One cooperative launch of dec_fused when every CTA of the grid can be
+// resident at once; otherwise the three-kernel sequence.
 template <int D>
-cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, float *z, float2 *part,
-                     float *opart, unsigned *err, cudaStream_t stream) {
+cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, int sms, float *z, float2 *part,
+                     float *opart, unsigned *sync, unsigned *err, cudaStream_t stream) {
     const int smem = (int)sizeof(DecSmem);
-    cudaError_t e = cudaFuncSetAttribute(dec_scores<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static PerDeviceOnce once;
+    int per_sm = 0;
+    cudaError_t e = per_device_once(once, &per_sm, [&](int &v) {
+        cudaError_t r = cudaFuncSetAttribute(dec_fused<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (r == cudaSuccess) r = cudaFuncSetAttribute(dec_scores<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (r == cudaSuccess) r = cudaFuncSetAttribute(dec_weights<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        return r != cudaSuccess ? r : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, dec_fused<D>, kDecBlock, smem);
+    });
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(dec_weights<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    if ((long long)nch * BH <= (long long)per_sm * sms) {
+        e = cudaMemsetAsync(sync, 0, (size_t)(1 + BH) * sizeof(unsigned), stream);
+        if (e != cudaSuccess) return e;
+        const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
+        const auto *k = static_cast<const __nv_bfloat16 *>(pr.k);
+        const auto *v = static_cast<const __nv_bfloat16 *>(pr.v);
+        auto *o = static_cast<__nv_bfloat16 *>(pr.out);
+        int L = pr.L, mode = pr.mode, p = pr.p;
+        void *args[] = {&q, &k, &v, &L, &chunk, &mode, &p, &part, &opart, &o, &sync, &err};
+        return cudaLaunchCooperativeKernel((const void *)dec_fused<D>, dim3(nch, BH), dim3(kDecBlock), args,
+                                           (size_t)smem, stream);
+    }
     const dim3 grid(nch, BH);
     const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
     const auto *k = static_cast<const __nv_bfloat16 *>(pr.k);
@@ -402,35 +577,46 @@ cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, float 
     return cudaGetLastError();
 }
 
+// Layout: [scores z: BH*L floats][chunk statistics][partials [BH][nch][d+1]]
+// [sync counters: 1 + BH]; each part 256-byte aligned.
+struct DecLayout {
+    size_t part, opart, sync, total;
+};
+
+DecLayout dec_layout(int BH, int L, int d, int nch) {
+    auto r = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    DecLayout l;
+    l.part = r((size_t)BH * L * 4);
+    l.opart = l.part + r((size_t)BH * nch * 8);
+    l.sync = l.opart + r((size_t)BH * nch * (d + 1) * 4);
+    l.total = l.sync + r((size_t)(1 + BH) * 4);
+    return l;
+}
+
 }  // namespace
 
 size_t decode_workspace_bytes(int BH, int L, int d, int sms) {
     const int chunk = choose_chunk(BH, L, sms);
-    const size_t nch = (L + chunk - 1) / chunk;
-    const size_t z = ((size_t)BH * L * 4 + 255) & ~(size_t)255;
-    const size_t part = ((size_t)BH * nch * 8 + 255) & ~(size_t)255;
-    const size_t op = (size_t)BH * nch * (d + 1) * 4;
-    return z + part + op;
+    return dec_layout(BH, L, d, (L + chunk - 1) / chunk).total;
 }
 
 cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream) {
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    int sms = 0;
+    cudaError_t e = device_sms(&sms);
     if (e != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     unsigned *err = nullptr;
     if ((e = error_word_ptr(&err)) != cudaSuccess) return e;
     const int BH = pr.B * pr.H;
     const int chunk = choose_chunk(BH, pr.L, sms);
     const int nch = (pr.L + chunk - 1) / chunk;
     char *base = static_cast<char *>(ws);
+    const DecLayout lay = dec_layout(BH, pr.L, pr.d, nch);
     float *z = reinterpret_cast<float *>(base);
-    const size_t zb = ((size_t)BH * pr.L * 4 + 255) & ~(size_t)255;
-    float2 *part = reinterpret_cast<float2 *>(base + zb);
-    const size_t pb = ((size_t)BH * nch * 8 + 255) & ~(size_t)255;
-    float *opart = reinterpret_cast<float *>(base + zb + pb);
-    return pr.d == 64 ? launch_d<64>(pr, BH, chunk, nch, z, part, opart, err, stream)
-                      : launch_d<128>(pr, BH, chunk, nch, z, part, opart, err, stream);
+    float2 *part = reinterpret_cast<float2 *>(base + lay.part);
+    float *opart = reinterpret_cast<float *>(base + lay.opart);
+    unsigned *sync = reinterpret_cast<unsigned *>(base + lay.sync);
+    return pr.d == 64 ? launch_d<64>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, stream)
+                      : launch_d<128>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, stream);
 }
 
 }  // namespace lssar

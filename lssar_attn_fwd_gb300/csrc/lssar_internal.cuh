@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 namespace lssar {
@@ -69,6 +70,44 @@ struct DecodeProblem {
 };
 size_t decode_workspace_bytes(int BH, int L, int d, int sms);
 cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream);
+
+// Launch-time setup that only has to happen once per device (function
+// attributes, occupancy queries): `fn(v)` returns a cudaError_t and stores
+// what it found in v; the first successful result is kept.
+struct PerDeviceOnce {
+    static constexpr int kMaxDevices = 64;
+    std::mutex mu;
+    bool done[kMaxDevices] = {};
+    int value[kMaxDevices] = {};
+};
+
+template <class F>
+cudaError_t per_device_once(PerDeviceOnce &once, int *value, F &&fn) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= PerDeviceOnce::kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(once.mu);
+    if (!once.done[dev]) {
+        int v = 0;
+        e = fn(v);
+        if (e != cudaSuccess) return e;
+        once.value[dev] = v;
+        once.done[dev] = true;
+    }
+    if (value) *value = once.value[dev];
+    return cudaSuccess;
+}
+
+// Number of SMs of the current device (queried once per device).
+inline cudaError_t device_sms(int *sms) {
+    static PerDeviceOnce once;
+    return per_device_once(once, sms, [](int &v) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        return e != cudaSuccess ? e : cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    });
+}
 
 // Reads and clears the device error word of the current device.
 cudaError_t read_and_clear_error_word(unsigned int *word);

@@ -188,9 +188,8 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
     prm.counter = counter;
     cudaError_t e = error_word_ptr(&prm.err);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int sms = 0;
+    if ((e = device_sms(&sms)) != cudaSuccess) return e;
     const int grid = prm.n_items < sms ? prm.n_items : sms;
     if (ev.main && (e = cudaEventRecord(ev.main, stream)) != cudaSuccess) return e;
     e = pr.d == 64 ? tc::dispatch_d64(pr, mq, mk, mv, prm, grid, stream)

@@ -34,6 +34,7 @@ def decode(torch, qb, kb, vb, p, mode):
     q_last = dev(qb[:, :, -1])
     out = api.lssar_attn_decode(q_last, dev(kb), dev(vb), p=p, mode=mode)
     torch.cuda.synchronize()
+    assert api.device_error_word() == 0
     return out.float().cpu().numpy().astype(np.float64)
 
 
@@ -73,3 +74,30 @@ def test_decode_equals_prefill_last_row(torch_mod):
     last = full[:, :, -1].float().cpu().numpy()
     got = decode(torch, qb, kb, vb, 15, MODE_LSSAR)
     assert np.abs(got - last).max() <= 5e-2
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_many_heads(torch_mod, d):
+    # 768 heads: more CTAs than can be resident at once, so the step runs as
+    # separate score / weight / combine launches instead of one cooperative
+    # launch; sampled heads against the oracle
+    B, H, L = 8, 96, 300
+    qb, kb, vb = make_qkv(B, H, L, d, seed=d)
+    for mode, p in [(MODE_LSSAR, 15), (MODE_SOFTMAX, 1)]:
+        got = decode(torch_mod, qb, kb, vb, p, mode)
+        for b, h in ((0, 0), (3, 50), (7, 95)):
+            qf, kf, vf = (bf16_bits_to_f64(t[b, h]) for t in (qb, kb, vb))
+            ref = attention_forward(qf, kf, vf, mode, p, rows=np.array([L]))[0]
+            assert np.abs(got[b, h] - ref).max() <= tol(mode, p), (d, mode, b, h)
+
+
+def test_decode_long_single_head(torch_mod):
+    # one head, 40000 keys: hundreds of chunks of one head meet at the grid
+    # barrier and the last one to finish combines them
+    B, H, L, d = 1, 1, 40000, 64
+    qb, kb, vb = make_qkv(B, H, L, d, seed=5)
+    qf, kf, vf = (bf16_bits_to_f64(t[0, 0]) for t in (qb, kb, vb))
+    for mode, p in [(MODE_LSSAR, 15), (MODE_SOFTMAX_RW, 3)]:
+        got = decode(torch_mod, qb, kb, vb, p, mode)
+        ref = attention_forward(qf, kf, vf, mode, p, rows=np.array([L]))[0]
+        assert np.abs(got[0, 0] - ref).max() <= tol(mode, p), mode
