@@ -206,8 +206,8 @@ __device__ __forceinline__ Elem element(float2 z, float2 m, float2 kappa, float2
         r.slope = make_float2(ptx::ex2(d.x), ptx::ex2(d.y));
     }
     if constexpr (is_reweight(MODE)) {
-        const float2 t = __ffma2_rn(b, kappa, beta);
-        const float2 base = make_float2(fmaxf(t.x, 0.f), fmaxf(t.y, 0.f));
+        // ReLU by a saturating FMA: b kappa + beta never exceeds 1 except by rounding
+        const float2 base = ptx::fma_sat2(b, kappa, beta);
         r.u = pow_pm1<PK>(base, p);
         r.w = __fmul2_rn(r.u, base);
     } else {

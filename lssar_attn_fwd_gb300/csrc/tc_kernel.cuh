@@ -338,9 +338,9 @@ __device__ __forceinline__ void weights_z(const uint32_t (&r)[32], const RowCons
                 const float2 v = __fadd2_rn(make_float2(ptx::ex2(z.x), ptx::ex2(z.y)), make_float2(1.f, 1.f));
                 phi = make_float2(ptx::rcp(v.x), ptx::rcp(v.y));
             }
-            const float2 t = __ffma2_rn(phi, make_float2(rc.kappa, rc.kappa),
-                                        make_float2(rc.beta, rc.beta));
-            w = powk2<PK>(make_float2(fmaxf(t.x, 0.f), fmaxf(t.y, 0.f)), p);
+            // ReLU of the re-weighting input by a saturating FMA: phi kappa + beta
+            // never exceeds 1 except by rounding (the row maximum maps to 1)
+            w = powk2<PK>(ptx::fma_sat2(phi, make_float2(rc.kappa, rc.kappa), make_float2(rc.beta, rc.beta)), p);
         }
         acc = __fadd2_rn(acc, w);
         pk[j / 2] = ptx::pack_bf16x2(w.x, w.y);

@@ -282,6 +282,14 @@ __device__ __forceinline__ float rcp(float x) {
     return y;
 }
 
+// a * b + c clamped to [0, 1] (one saturating FMA), two lanes.
+__device__ __forceinline__ float2 fma_sat2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d.x) : "f"(a.x), "f"(b.x), "f"(c.x));
+    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d.y) : "f"(a.y), "f"(b.y), "f"(c.y));
+    return d;
+}
+
 // Two floats to packed bf16x2 (round to nearest even): lo in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
