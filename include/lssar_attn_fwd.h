@@ -223,6 +223,17 @@ int lssar_attn_fwd_profiled(const void *q, const void *k, const void *v, void *o
 int lssar_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *out,
                            int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
 
+/*
+ * TEST ONLY: the failure path of the bounded waits.  Runs one decode step
+ * (B=1 H=4 L=512 d=64, zero inputs, internal scratch) whose producer warps
+ * withhold every copy, so that each wait of that launch gives up after its
+ * 2 s bound: the kernel records decode code 41 in the device error word,
+ * leaves its loops and ends without a fault (no copy is in flight).  Takes
+ * about 2 s on the GPU; returns LSSAR_OK once launched, LSSAR_ERR_CUDA
+ * otherwise.  Read the code with lssar_device_error_word afterwards.
+ */
+int lssar_selftest_stall(cudaStream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *lssar_status_string(int status);
 

@@ -24,6 +24,7 @@ _EXPORTS = (
     "lssar_attn_fwd_train",
     "lssar_attn_bwd",
     "lssar_attn_bwd_simt",
+    "lssar_selftest_stall",
     "lssar_status_string",
     "lssar_device_error_word",
     "lssar_abi_version",
@@ -67,6 +68,8 @@ def load_library():
         fn.restype = ctypes.c_int
     lib.lssar_attn_fwd_profiled.argtypes = fwd_args + [ctypes.c_void_p] * 3
     lib.lssar_attn_fwd_profiled.restype = ctypes.c_int
+    lib.lssar_selftest_stall.argtypes = [ctypes.c_void_p]
+    lib.lssar_selftest_stall.restype = ctypes.c_int
     lib.lssar_status_string.argtypes = [ctypes.c_int]
     lib.lssar_status_string.restype = ctypes.c_char_p
     lib.lssar_device_error_word.argtypes = [ctypes.POINTER(ctypes.c_uint)]
@@ -271,6 +274,13 @@ def lssar_attn_fwd_profiled(q, k, v, p, mode, out, stream, ev_start, ev_main, ev
         ctypes.c_void_p(ev_end.cuda_event))
     _check(status)
     return out
+
+
+def selftest_stall():
+    """Test only: launches a decode step whose copies are withheld, so that its
+    bounded waits give up (about 2 s); read the code with device_error_word()."""
+    import torch
+    _check(load_library().lssar_selftest_stall(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
 
 
 def device_error_word():

@@ -245,6 +245,31 @@ int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out, 
     return lssar::launch_simt(pr, stream) == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
 }
 
+int lssar_selftest_stall(cudaStream_t stream) {
+    // B=1 H=4 L=512 d=64, zero inputs, from the pool
+    const int B = 1, H = 4, L = 512, d = 64;
+    const size_t cache = (size_t)B * H * L * d * 2;
+    int sms = 0;
+    if (lssar::device_sms(&sms) != cudaSuccess) return LSSAR_ERR_CUDA;
+    const size_t ws_bytes = lssar::decode_workspace_bytes(B * H, L, d, sms);
+    cudaMemPool_t pool;
+    if (device_pool(&pool) != cudaSuccess) return LSSAR_ERR_CUDA;
+    void *buf = nullptr;
+    // [q: B*H*d bf16][k cache][v cache][out: B*H*d bf16][decode scratch], 1 KiB-aligned parts
+    const size_t qbytes = (size_t)B * H * d * 2;
+    const size_t off_k = 1024, off_v = off_k + cache, off_o = off_v + cache, off_ws = off_o + 1024;
+    if (qbytes > 1024) return LSSAR_ERR_SHAPE;
+    if (cudaMallocFromPoolAsync(&buf, off_ws + ws_bytes, pool, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    char *b = static_cast<char *>(buf);
+    cudaError_t e = cudaMemsetAsync(b, 0, off_ws, stream);
+    if (e == cudaSuccess) {
+        lssar::DecodeProblem pr{b, b + off_k, b + off_v, b + off_o, B, H, L, d, 3, LSSAR_MODE_LSSAR};
+        e = lssar::launch_decode(pr, b + off_ws, stream, true);
+    }
+    if (cudaFreeAsync(buf, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
+}
+
 const char *lssar_status_string(int status) {
     switch (status) {
         case LSSAR_OK: return "ok";

@@ -70,7 +70,7 @@ enum Pass : int { kRowPass = 0, kColPass = 1 };
 
 // Error codes in the device error word (the forward kernel uses 1-11).
 enum : unsigned { kErrXFull = 21, kErrXEmpty, kErrRingFull, kErrRingEmpty, kErrSFull, kErrSFree,
-                  kErrAFull, kErrAFree, kErrAccFull, kErrAccFree, kErrItem, kErrRed };
+                  kErrAFull, kErrAFree, kErrAccFull, kErrAccFree, kErrItem, kErrRed, kErrDrain };
 
 constexpr uint32_t kKmajorLbo = 16, kKmajorSbo = 1024;    // K-major tiles
 constexpr uint32_t kMnLbo = 16384, kMnSbo = 1024;         // the same tiles read MN-major
@@ -124,14 +124,16 @@ struct __align__(8) Barriers {
 };
 static_assert(sizeof(Barriers) <= 12288, "barrier block too large");
 
+// Bounded wait on an mbarrier phase; with honour_abort it also gives up as
+// soon as another role of the CTA has raised the abort flag.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Barriers *b, unsigned *err,
-                                         unsigned code) {
+                                         unsigned code, bool honour_abort = true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
         if (ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
         if ((spin & 15u) == 0) {
-            if (*(volatile int *)&b->abort_flag) return false;
+            if (honour_abort && *(volatile int *)&b->abort_flag) return false;
             if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
                 atomicCAS(err, 0u, code);
                 *(volatile int *)&b->abort_flag = 1;
@@ -366,6 +368,12 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                     }
                 }
             }
+            // No copy may be in flight when the CTA ends, also after an abort:
+            // wait (bounded) until the last stages and anchor tiles issued have landed.
+            for (uint32_t i = ring_idx > (uint32_t)NS ? ring_idx - NS : 0; i < ring_idx; ++i)
+                wait_bar(ptx::smem_u32(&bars->ring_full[i % NS]), (i / NS) & 1, bars, prm.err, kErrDrain, false);
+            if (x_cnt > 0)
+                wait_bar(ptx::smem_u32(&bars->x_full), (x_cnt - 1) & 1, bars, prm.err, kErrDrain, false);
         }
         __syncwarp();
     } else if (warp == 1) {

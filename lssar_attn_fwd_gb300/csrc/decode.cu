@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kDecBlock, kDecCtasPerSm)
 dec_fused(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
           const __nv_bfloat16 *__restrict__ v, int L, int chunk, int mode, int p,
           float2 *__restrict__ part, float *__restrict__ opart, __nv_bfloat16 *__restrict__ out,
-          unsigned *__restrict__ sync, unsigned *err) {
+          unsigned *__restrict__ sync, unsigned *err, int withhold_copies) {
     extern __shared__ __align__(128) uint8_t dsm[];
     DecSmem *sm = reinterpret_cast<DecSmem *>(dsm);
     __shared__ float qs[D];
@@ -435,8 +435,11 @@ dec_fused(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__
     const int n_st = rk.stages();
     const Ring<D> rv{sm, v + ((size_t)bh * L + j0) * D, n, err, n_st};
     init_ring(sm);
+    // withhold_copies (self-test of the failure path only): the producer
+    // issues nothing, so every consumer wait runs into its bound
+    const int n_issue = withhold_copies ? 0 : n_st;
     int issued_k = 0, issued_v = 0;
-    if (producer && lane == 0) issued_k = rk.issue_upto(0, min(n_st, kDecStages));
+    if (producer && lane == 0) issued_k = rk.issue_upto(0, min(n_issue, kDecStages));
     // phase A: scores
     float qss = 0.f;
     for (int t = threadIdx.x; t < D; t += kDecBlock) {
@@ -451,7 +454,7 @@ dec_fused(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__
     float m = -INFINITY;
     if (producer) {
         if (lane == 0) {
-            issued_k = rk.issue_upto(issued_k, n_st);
+            issued_k = rk.issue_upto(issued_k, n_issue);
             // the first value stages follow as the consumers free the ring
             if (issued_k == n_st) issued_v = rv.issue_upto(0, min(n_st, kDecStages));
         }
@@ -544,7 +547,7 @@ int choose_chunk(int BH, int L, int sms) {
 // resident at once; otherwise the three-kernel sequence.
 template <int D>
 cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, int sms, float *z, float2 *part,
-                     float *opart, unsigned *sync, unsigned *err, cudaStream_t stream) {
+                     float *opart, unsigned *sync, unsigned *err, int withhold, cudaStream_t stream) {
     const int smem = (int)sizeof(DecSmem);
     static PerDeviceOnce once;
     int per_sm = 0;
@@ -555,6 +558,7 @@ cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, int sm
         return r != cudaSuccess ? r : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, dec_fused<D>, kDecBlock, smem);
     });
     if (e != cudaSuccess) return e;
+    if (withhold && (long long)nch * BH > (long long)per_sm * sms) return cudaErrorInvalidConfiguration;
     if ((long long)nch * BH <= (long long)per_sm * sms) {
         e = cudaMemsetAsync(sync, 0, (size_t)(1 + BH) * sizeof(unsigned), stream);
         if (e != cudaSuccess) return e;
@@ -563,7 +567,7 @@ cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, int sm
         const auto *v = static_cast<const __nv_bfloat16 *>(pr.v);
         auto *o = static_cast<__nv_bfloat16 *>(pr.out);
         int L = pr.L, mode = pr.mode, p = pr.p;
-        void *args[] = {&q, &k, &v, &L, &chunk, &mode, &p, &part, &opart, &o, &sync, &err};
+        void *args[] = {&q, &k, &v, &L, &chunk, &mode, &p, &part, &opart, &o, &sync, &err, &withhold};
         return cudaLaunchCooperativeKernel((const void *)dec_fused<D>, dim3(nch, BH), dim3(kDecBlock), args,
                                            (size_t)smem, stream);
     }
@@ -600,7 +604,7 @@ size_t decode_workspace_bytes(int BH, int L, int d, int sms) {
     return dec_layout(BH, L, d, (L + chunk - 1) / chunk).total;
 }
 
-cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream, bool withhold_copies) {
     int sms = 0;
     cudaError_t e = device_sms(&sms);
     if (e != cudaSuccess) return e;
@@ -615,8 +619,9 @@ cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream
     float2 *part = reinterpret_cast<float2 *>(base + lay.part);
     float *opart = reinterpret_cast<float *>(base + lay.opart);
     unsigned *sync = reinterpret_cast<unsigned *>(base + lay.sync);
-    return pr.d == 64 ? launch_d<64>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, stream)
-                      : launch_d<128>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, stream);
+    const int w = withhold_copies ? 1 : 0;
+    return pr.d == 64 ? launch_d<64>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, w, stream)
+                      : launch_d<128>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, w, stream);
 }
 
 }  // namespace lssar

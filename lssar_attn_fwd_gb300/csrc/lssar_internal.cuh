@@ -69,7 +69,9 @@ struct DecodeProblem {
     int B, H, L, d, p, mode;
 };
 size_t decode_workspace_bytes(int BH, int L, int d, int sms);
-cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream);
+// withhold_copies: self-test of the failure path (the one-launch kernel issues
+// no copies, every wait of the launch runs into its bound).
+cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream, bool withhold_copies = false);
 
 // Launch-time setup that only has to happen once per device (function
 // attributes, occupancy queries): `fn(v)` returns a cudaError_t and stores

@@ -85,7 +85,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a stuck wait gives up after
 
 // Error codes written to the device error word (first failure wins).
 enum : unsigned { kErrQFull = 1, kErrQEmpty, kErrKvFull, kErrKvEmpty, kErrSFull, kErrSFree,
-                  kErrOFull, kErrOFree, kErrItem, kErrPFull, kErrPFree };
+                  kErrOFull, kErrOFree, kErrItem, kErrPFull, kErrPFree, kErrDrain };
 
 // Shared-memory descriptor strides.  K-major tiles (Q, K): rows of 128 bytes,
 // 8-row groups 1024 bytes apart.  MN-major V tiles: 16 keys per MMA = 2048
@@ -151,14 +151,16 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 
 constexpr uint32_t kSuspendNs = 1000000;   // hardware suspend per try_wait (upper bound)
 
+// Bounded wait on an mbarrier phase; with honour_abort it also gives up as
+// soon as another role of the CTA has raised the abort flag.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Barriers *b, unsigned *err,
-                                         unsigned code) {
+                                         unsigned code, bool honour_abort = true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t spin = 1;; ++spin) {
         if (ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
         if ((spin & 15u) == 0) {
-            if (*(volatile int *)&b->abort_flag) return false;
+            if (honour_abort && *(volatile int *)&b->abort_flag) return false;
             if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
                 atomicCAS(err, 0u, code);
                 *(volatile int *)&b->abort_flag = 1;
@@ -487,6 +489,12 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if (ok) ok = push(&tmV, kt, bh);
                 }
             }
+            // No copy may be in flight when the CTA ends, also after an abort:
+            // wait (bounded) until the last stages and Q tiles issued have landed.
+            for (uint32_t i = ring_idx > (uint32_t)NS ? ring_idx - NS : 0; i < ring_idx; ++i)
+                wait_bar(ptx::smem_u32(&bars->kv_full[i % NS]), (i / NS) & 1, bars, prm.err, kErrDrain, false);
+            if (q_cnt > 0)
+                wait_bar(ptx::smem_u32(&bars->q_full), (q_cnt - 1) & 1, bars, prm.err, kErrDrain, false);
         }
         __syncwarp();
     } else if (warp == 1) {
