@@ -224,6 +224,17 @@ int lssar_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *ou
                            int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
 
 /*
+ * Introspection of the attention kernel's work schedule (host only, no CUDA
+ * call).  Work items are pairs of 128-row Q tiles of one head, numbered
+ * longest first (item i: head i % BH, pair n_pairs - 1 - i / BH).  CTA c of a
+ * grid of `grid` CTAs first processes first[2c] and then first[2c+1] (-1:
+ * none), then the items from *tail_base on, as a global counter hands them
+ * out.  first must hold 2*grid ints; 1 <= grid <= 256.  Returns LSSAR_OK,
+ * LSSAR_ERR_NULL or LSSAR_ERR_SHAPE.
+ */
+int lssar_schedule_plan(int BH, int n_qtiles, int grid, int *first, int *tail_base);
+
+/*
  * TEST ONLY: the failure path of the bounded waits.  Runs one decode step
  * (B=1 H=4 L=512 d=64, zero inputs, internal scratch) whose producer warps
  * withhold every copy, so that each wait of that launch gives up after its

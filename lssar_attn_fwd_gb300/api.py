@@ -25,6 +25,7 @@ _EXPORTS = (
     "lssar_attn_bwd",
     "lssar_attn_bwd_simt",
     "lssar_selftest_stall",
+    "lssar_schedule_plan",
     "lssar_status_string",
     "lssar_device_error_word",
     "lssar_abi_version",
@@ -68,6 +69,8 @@ def load_library():
         fn.restype = ctypes.c_int
     lib.lssar_attn_fwd_profiled.argtypes = fwd_args + [ctypes.c_void_p] * 3
     lib.lssar_attn_fwd_profiled.restype = ctypes.c_int
+    lib.lssar_schedule_plan.argtypes = [ctypes.c_int] * 3 + [ctypes.POINTER(ctypes.c_int)] * 2
+    lib.lssar_schedule_plan.restype = ctypes.c_int
     lib.lssar_selftest_stall.argtypes = [ctypes.c_void_p]
     lib.lssar_selftest_stall.restype = ctypes.c_int
     lib.lssar_status_string.argtypes = [ctypes.c_int]

@@ -245,6 +245,11 @@ int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out, 
     return lssar::launch_simt(pr, stream) == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
 }
 
+int lssar_schedule_plan(int BH, int n_qtiles, int grid, int *first, int *tail_base) {
+    if (!first || !tail_base) return LSSAR_ERR_NULL;
+    return lssar::schedule_plan(BH, n_qtiles, grid, first, tail_base) == 0 ? LSSAR_OK : LSSAR_ERR_SHAPE;
+}
+
 int lssar_selftest_stall(cudaStream_t stream) {
     // B=1 H=4 L=512 d=64, zero inputs, from the pool
     const int B = 1, H = 4, L = 512, d = 64;

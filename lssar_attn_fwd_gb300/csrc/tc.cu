@@ -4,7 +4,13 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <functional>
+#include <map>
 #include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
 
 #include "tc_kernel.cuh"
 #include "tc_dispatch.cuh"
@@ -133,6 +139,90 @@ cudaError_t error_word_ptr(unsigned **out) {
 }
 
 namespace {
+
+// Work schedule of the attention kernel for BH heads of n_qtiles Q tiles on
+// `grid` CTAs.  Item id i (longest first) is the Q-tile pair m = n_pairs-1 -
+// i/BH of head i%BH; its cost is modelled as the K tiles its two Q tiles
+// stream, (2m+1) + (2m+2) (one fewer tile when the second is past the end),
+// plus one tile of fixed cost.  Two schedules are simulated and the one with
+// the shorter makespan is used:
+//   longest first: CTA c starts with item c, the rest from the counter;
+//   complements:   CTA c starts with item c and its complement h0 - c, where
+//                  h0 is the first item that fits next to item 0 within the
+//                  mean load; items h0+1.. follow from the counter.
+struct Schedule {
+    int tail_base = 0;
+    std::vector<int> first;   // 2 per CTA, -1 for none
+};
+
+Schedule plan_schedule(int BH, int n_qtiles, int grid) {
+    const int n_pairs = (n_qtiles + 1) / 2;
+    const long long N = (long long)BH * n_pairs;
+    auto cost = [&](long long id) {
+        const int m = n_pairs - 1 - (int)(id / BH);
+        const int qa = 2 * m, qb = 2 * m + 1;
+        return (double)(qa + 1) + (qb < n_qtiles ? qb + 1 : 0) + 1.0;
+    };
+    // makespan of: per-CTA preloaded work, then items [tail, N) longest first
+    auto simulate = [&](std::vector<double> load, long long tail) {
+        std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>,
+                            std::greater<std::pair<double, int>>> heap;
+        for (int c = 0; c < grid; ++c) heap.push({load[c], c});
+        for (long long i = tail; i < N; ++i) {
+            auto t = heap.top();
+            heap.pop();
+            t.first += cost(i);
+            load[t.second] = t.first;
+            heap.push(t);
+        }
+        return *std::max_element(load.begin(), load.end());
+    };
+    Schedule lpt;
+    lpt.first.assign(2 * (size_t)grid, -1);
+    std::vector<double> load(grid, 0.0);
+    for (int c = 0; c < grid && c < N; ++c) {
+        lpt.first[2 * c] = c;
+        load[c] = cost(c);
+    }
+    lpt.tail_base = (int)std::min<long long>(grid, N);
+    const double lpt_span = simulate(load, lpt.tail_base);
+    double total = 0.0;
+    for (long long i = 0; i < N; ++i) total += cost(i);
+    const double mean = total / grid;
+    long long h0 = -1;
+    for (long long h = 1; h < N; ++h)
+        if (cost(0) + cost(h) <= mean) {
+            h0 = h;
+            break;
+        }
+    if (h0 < 0 || (h0 + 2) / 2 > grid) return lpt;
+    Schedule cmp;
+    cmp.first.assign(2 * (size_t)grid, -1);
+    std::fill(load.begin(), load.end(), 0.0);
+    for (long long c = 0; c <= h0 - c; ++c) {
+        cmp.first[2 * c] = (int)c;
+        load[c] = cost(c);
+        if (h0 - c != c) {
+            cmp.first[2 * c + 1] = (int)(h0 - c);
+            load[c] += cost(h0 - c);
+        }
+    }
+    cmp.tail_base = (int)(h0 + 1);
+    return simulate(load, cmp.tail_base) < lpt_span ? cmp : lpt;
+}
+
+// Schedules are computed once per (BH, n_qtiles, grid).
+std::mutex g_plan_mutex;
+std::map<std::tuple<int, int, int>, Schedule> g_plans;
+
+const Schedule &schedule_for(int BH, int n_qtiles, int grid) {
+    std::lock_guard<std::mutex> lock(g_plan_mutex);
+    const auto key = std::make_tuple(BH, n_qtiles, grid);
+    auto it = g_plans.find(key);
+    if (it == g_plans.end()) it = g_plans.emplace(key, plan_schedule(BH, n_qtiles, grid)).first;
+    return it->second;
+}
+
 constexpr size_t kCounterBytes = 256;
 
 size_t qk_bytes(const Problem &pr) {
@@ -190,13 +280,28 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
     if (e != cudaSuccess) return e;
     int sms = 0;
     if ((e = device_sms(&sms)) != cudaSuccess) return e;
-    const int grid = prm.n_items < sms ? prm.n_items : sms;
+    int grid = prm.n_items < sms ? prm.n_items : sms;
+    if (grid > tc::kMaxCtas) grid = tc::kMaxCtas;
+    const Schedule &sch = schedule_for(BH, prm.n_qtiles, grid);
+    prm.tail_base = sch.tail_base;
+    for (int c = 0; c < tc::kMaxCtas; ++c) {
+        prm.first_items[c][0] = c < grid ? sch.first[2 * c] : -1;
+        prm.first_items[c][1] = c < grid ? sch.first[2 * c + 1] : -1;
+    }
     if (ev.main && (e = cudaEventRecord(ev.main, stream)) != cudaSuccess) return e;
     e = pr.d == 64 ? tc::dispatch_d64(pr, mq, mk, mv, prm, grid, stream)
                    : tc::dispatch_d128(pr, mq, mk, mv, prm, grid, stream);
     if (e != cudaSuccess) return e;
     if (ev.end) e = cudaEventRecord(ev.end, stream);
     return e;
+}
+
+int schedule_plan(int BH, int n_qtiles, int grid, int *first, int *tail_base) {
+    if (BH < 1 || n_qtiles < 1 || grid < 1 || grid > tc::kMaxCtas) return -1;
+    const Schedule &sch = schedule_for(BH, n_qtiles, grid);
+    for (int i = 0; i < 2 * grid; ++i) first[i] = sch.first[i];
+    *tail_base = sch.tail_base;
+    return 0;
 }
 
 cudaError_t read_and_clear_error_word(unsigned int *word) {

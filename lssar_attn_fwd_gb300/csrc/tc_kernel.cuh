@@ -54,10 +54,12 @@
 // A work item is a pair of consecutive 128-row Q tiles of one head (2m, 2m+1)
 // sharing every K/V tile load; the two warpgroups ping-pong so that the MMA
 // of one tile overlaps the elementwise work of the other.  Items are numbered
-// longest first; each CTA starts with item blockIdx.x and then takes the next
-// unclaimed item from a global counter (longest-processing-time-first), the
-// producer warp publishing each item to the other roles through a small
-// shared-memory queue.
+// longest first.  Each CTA first works through up to two items fixed by the
+// host (a long item and its complement, so that the CTAs' loads come out
+// nearly equal), then takes the next unclaimed item of the remaining tail
+// from a global counter (longest-processing-time-first); without a plan the
+// fixed item is item blockIdx.x.  The producer warp publishes each item to
+// the other roles through a small shared-memory queue.
 // Causal masking: on the diagonal tile the scaled scores above the diagonal
 // are replaced by -inf, for which every weight below evaluates to exactly 0.
 // TMEM (512 columns): S0 [0,128), S1 [128,256); d = 64: P0 [256,320), P1 [320,384),
@@ -96,6 +98,7 @@ constexpr uint32_t kVLbo = 16384;
 constexpr uint32_t kVSbo = 1024;
 
 constexpr int kMaxHeadsP = 256;   // per-head exponents carried in the kernel parameters
+constexpr int kMaxCtas = 256;     // CTAs with a fixed first work list (one per SM)
 
 struct Params {
     int BH;          // B * H
@@ -108,6 +111,11 @@ struct Params {
     int H;           // heads per batch entry (for the per-head exponents)
     int per_head;    // 1: head h uses p_head[h] (generic power path only)
     int p_head[kMaxHeadsP];
+    // Work schedule: CTA c first processes first_items[c][0], then
+    // first_items[c][1] (-1: none), then items tail_base, tail_base + 1, ...
+    // as a global counter hands them out (items are numbered longest first).
+    int tail_base;
+    int first_items[kMaxCtas][2];
     __nv_bfloat16 *out;
     float4 *stats;       // per-row {m, kappa, beta, W} for the backward pass, or null
     unsigned *err;       // device error word
@@ -453,8 +461,8 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             while (ok) {
                 // claim and publish the next work item
                 const uint32_t s = qi % kItemQ, use = qi / kItemQ;
-                const int item = qi == 0 ? (int)blockIdx.x
-                                         : (int)(gridDim.x + atomicAdd(prm.counter, 1u));
+                const int fixed = qi < 2 ? prm.first_items[blockIdx.x][qi] : -1;
+                const int item = fixed >= 0 ? fixed : (int)(prm.tail_base + atomicAdd(prm.counter, 1u));
                 ++qi;
                 if (use > 0 && !wait_bar(ptx::smem_u32(&bars->item_empty[s]), (use - 1) & 1, bars,
                                          prm.err, kErrItem))

@@ -165,3 +165,42 @@ def test_backward_invalid_arguments(lib, name):
     assert c(6, DOUT) == -8                           # dk over dout
     assert c(7, STATS) == -8                          # dv over the stats
     assert c(6, DQ + 256) == -8                       # dk overlaps dq
+
+
+@pytest.mark.parametrize("BH,n_qtiles,grid", [(12, 64, 152), (96, 8, 152), (64, 32, 152), (12, 128, 152),
+                                              (8, 64, 152), (1, 1, 1), (3, 5, 7), (5, 63, 152), (200, 2, 152)])
+def test_schedule_covers_every_item_once(lib, BH, n_qtiles, grid):
+    n_pairs = (n_qtiles + 1) // 2
+    n_items = BH * n_pairs
+    grid = min(grid, n_items)
+    first = (ctypes.c_int * (2 * grid))()
+    tail = ctypes.c_int(0)
+    assert lib.lssar_schedule_plan(BH, n_qtiles, grid, first, ctypes.byref(tail)) == 0
+    fixed = [x for x in first if x >= 0]
+    assert len(fixed) == len(set(fixed))
+    # the fixed items are exactly [0, tail); the counter serves [tail, n_items)
+    assert sorted(fixed) == list(range(tail.value))
+    assert 0 < tail.value <= n_items
+    # every CTA's first fixed item (if any) is in slot 0
+    assert all(first[2 * c] >= 0 or first[2 * c + 1] < 0 for c in range(grid))
+
+
+def test_schedule_pairs_long_with_short_items(lib):
+    # 12 heads of 8192 rows (64 Q tiles, 32 pairs) on 152 CTAs: the long items
+    # come with complements, and the largest planned load is near the mean
+    BH, n_qtiles, grid = 12, 64, 152
+    first = (ctypes.c_int * (2 * grid))()
+    tail = ctypes.c_int(0)
+    assert lib.lssar_schedule_plan(BH, n_qtiles, grid, first, ctypes.byref(tail)) == 0
+    cost = lambda i: 4 * (31 - i // BH) + 3   # noqa: E731  K tiles of the pair's two Q tiles
+    loads = [sum(cost(x) for x in (first[2 * c], first[2 * c + 1]) if x >= 0) for c in range(grid)]
+    mean = sum(cost(i) for i in range(BH * 32)) / grid
+    assert tail.value > grid and max(loads) <= 1.02 * mean
+
+
+def test_schedule_rejects_bad_arguments(lib):
+    first = (ctypes.c_int * 2)()
+    tail = ctypes.c_int(0)
+    assert lib.lssar_schedule_plan(0, 4, 1, first, ctypes.byref(tail)) == -2
+    assert lib.lssar_schedule_plan(1, 4, 300, first, ctypes.byref(tail)) == -2
+    assert lib.lssar_schedule_plan(1, 4, 1, None, ctypes.byref(tail)) == -1
