@@ -274,7 +274,10 @@ __device__ __forceinline__ void to_z(uint32_t (&r)[32], int col0, int t, float a
 // The product form needs one FFMA per element instead of a log2: every factor
 // lies in (1, 2], so up to 64 factors multiply in fp32 without overflow (the
 // caller takes log2 of each 64-factor product once per tile).
-template <int MODE>
+// Off the diagonal tile (DIAG = false, no masked column) the positive part is
+// summed as (z - (-|z|)) / 2 with the -|z| the exponential needs anyway: two
+// packed FMAs per pair instead of two max and a packed add.
+template <int MODE, bool DIAG>
 __device__ __forceinline__ void stats_z(const uint32_t (&r)[32], float2 &relu_acc, float2 &prod,
                                         float &m) {
 #pragma unroll
@@ -289,9 +292,15 @@ __device__ __forceinline__ void stats_z(const uint32_t (&r)[32], float2 &relu_ac
             m = max3(m, z.x, z.y);
         }
         if constexpr (MODE == kLssar) {
-            const float2 u = make_float2(ptx::ex2(-fabsf(z.x)), ptx::ex2(-fabsf(z.y)));
+            const float2 nz = make_float2(-fabsf(z.x), -fabsf(z.y));
+            const float2 u = make_float2(ptx::ex2(nz.x), ptx::ex2(nz.y));
             prod = __ffma2_rn(prod, u, prod);
-            relu_acc = __fadd2_rn(relu_acc, make_float2(fmaxf(z.x, 0.f), fmaxf(z.y, 0.f)));
+            if constexpr (DIAG) {
+                relu_acc = __fadd2_rn(relu_acc, make_float2(fmaxf(z.x, 0.f), fmaxf(z.y, 0.f)));
+            } else {
+                const float2 twice = __ffma2_rn(nz, make_float2(-1.f, -1.f), z);   // z + |z|
+                relu_acc = __ffma2_rn(twice, make_float2(0.5f, 0.5f), relu_acc);
+            }
         }
     }
 }
@@ -730,8 +739,13 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         softmax_tile_stats(r[0], r[1], sm_run, sm_sum);
                     } else {
                         float2 prod[2] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
-                        stats_z<MODE>(r[0], acc[0], prod[0], mx[0]);
-                        stats_z<MODE>(r[1], acc[1], prod[1], mx[1]);
+                        if (kt == qt) {
+                            stats_z<MODE, true>(r[0], acc[0], prod[0], mx[0]);
+                            stats_z<MODE, true>(r[1], acc[1], prod[1], mx[1]);
+                        } else {
+                            stats_z<MODE, false>(r[0], acc[0], prod[0], mx[0]);
+                            stats_z<MODE, false>(r[1], acc[1], prod[1], mx[1]);
+                        }
                         if constexpr (MODE == kLssar)
                             s1_log += ptx::lg2((prod[0].x * prod[0].y) * (prod[1].x * prod[1].y));
                     }
