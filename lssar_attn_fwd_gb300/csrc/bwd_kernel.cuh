@@ -25,6 +25,9 @@
 //     one pass over the query tiles i >= j: S^T = Kh Qh^T, dP^T = V dO^T,
 //     P^T and ds^T / R -> TMEM, dV += P^T dO, dKh += (ds^T / R) Qh.  The
 //     query records arrive with each tile (bulk copy into the stage).
+// In the normalised modes the prologue writes the query rows as a_i qh_i
+// (fp16), exactly as the forward does, so S is z itself; the column pass's
+// product with those rows then takes ds_ij / a_i.
 // The same stage tile serves as the K-major B operand of a score product and
 // as the MN-major B operand of an accumulation (the 128B-swizzled TMA layout
 // is both); ds is rounded to the score operands' type (fp16 for the
@@ -184,6 +187,16 @@ struct Elem {
     float2 w;       // the weight
     float2 slope;   // dphi/dz
 };
+
+// z of a pair of scores: the normalised modes' query rows carry the length
+// scale already (the prologue writes a_i qh_i), so S is z; the softmax
+// normalisers scale raw q.k by a = log2(e) / sqrt(d).
+template <int MODE>
+__device__ __forceinline__ float2 score_z(uint32_t s0, uint32_t s1, float a) {
+    const float2 s = make_float2(__uint_as_float(s0), __uint_as_float(s1));
+    if constexpr (uses_normalised_qk(MODE)) return s;
+    else return __fmul2_rn(s, make_float2(a, a));
+}
 
 // Two elements (one per lane of the float2), each with its own row constants.
 template <int MODE, int PK>
@@ -576,8 +589,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 auto stats_tile = [&](const uint32_t (&rs)[32], const uint32_t (&rd)[32], auto diag) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
-                        const float2 z = __fmul2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])),
-                                                    make_float2(a, a));
+                        const float2 z = score_z<MODE>(rs[c], rs[c + 1], a);
                         float2 dP = make_float2(__uint_as_float(rd[c]), __uint_as_float(rd[c + 1]));
                         Elem el = element<MODE, PK>(z, mm, kk, bb, pe);
                         float2 lo = dP, hi = dP;
@@ -626,19 +638,21 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 if (g == 0) {
                     // the column pass's record of this query, field-major per tile
                     // (all zero past L: no contribution)
-                    const float fld[8] = {a, st.x, st.y, st.z, 1.f / st.w, a * F, Di, a * dS1};
+                    // normalised modes: the column pass multiplies by the scaled
+                    // query rows a_i qh_i, so its ds omits a_i (dscale = 1)
+                    const float dscale = kRaw ? a : 1.f;
+                    const float fld[8] = {a, st.x, st.y, st.z, 1.f / st.w, dscale * F, Di, dscale * dS1};
                     float *rec = prm.rowc + ((size_t)bh * prm.n_tiles + at) * 8 * kBN + t;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) rec[k * kBN] = valid ? fld[k] : 0.f;
-                    if (valid) atomicMax(prm.rmax + bh, __float_as_uint(a * (F * dev + fabsf(dS1))));
+                    if (valid) atomicMax(prm.rmax + bh, __float_as_uint(dscale * (F * dev + fabsf(dS1))));
                 }
                 // pass 2: ds / r into TMEM, dqh accumulates in Acc1
                 auto ds_tile = [&](const uint32_t (&rs)[32], const uint32_t (&rd)[32], uint32_t (&w1)[16],
                                    auto diag) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
-                        const float2 z = __fmul2_rn(make_float2(__uint_as_float(rs[c]), __uint_as_float(rs[c + 1])),
-                                                    make_float2(a, a));
+                        const float2 z = score_z<MODE>(rs[c], rs[c + 1], a);
                         const float2 dP = make_float2(__uint_as_float(rd[c]), __uint_as_float(rd[c + 1]));
                         const Elem el = element<MODE, PK>(z, mm, kk, bb, pe);
                         const float2 dd = __fadd2_rn(dP, make_float2(-Di, -Di));
@@ -696,17 +710,20 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                         float4 f[8];
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
-                            if (k != 1 || MODE == kSoftmax || MODE == kSoftmaxRw)
+                            if (k > 1 || kRaw)   // a and m: softmax normalisers only
                                 f[k] = *reinterpret_cast<const float4 *>(rec + k * kBN + q0);
-                        // fields: 0 a, 1 m, 2 kappa, 3 beta, 4 1/W, 5 a F, 6 D, 7 a dS1
+                        // fields: 0 a, 1 m, 2 kappa, 3 beta, 4 1/W, 5 s F, 6 D, 7 s dS1, with
+                        // s = a for the softmax normalisers and 1 for the normalised modes
+                        // (their query operand carries a_i)
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             auto pick = [&](int k) {
                                 return h == 0 ? make_float2(f[k].x, f[k].y) : make_float2(f[k].z, f[k].w);
                             };
                             const int cc = c + 2 * h;
-                            const float2 z = __fmul2_rn(make_float2(__uint_as_float(rs[cc]), __uint_as_float(rs[cc + 1])),
-                                                        pick(0));
+                            const float2 z = kRaw ? __fmul2_rn(make_float2(__uint_as_float(rs[cc]),
+                                                                           __uint_as_float(rs[cc + 1])), pick(0))
+                                                  : make_float2(__uint_as_float(rs[cc]), __uint_as_float(rs[cc + 1]));
                             const float2 dP = make_float2(__uint_as_float(rd[cc]), __uint_as_float(rd[cc + 1]));
                             const float2 mcol = (MODE == kSoftmax || MODE == kSoftmaxRw) ? pick(1) : make_float2(0.f, 0.f);
                             const Elem el = element<MODE, PK>(z, mcol, pick(2), pick(3), pe);

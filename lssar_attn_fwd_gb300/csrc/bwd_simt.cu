@@ -21,17 +21,19 @@
 //   dq_i  = (dqh_i - qh_i (qh_i . dqh_i)) / |q_i|   (normalised modes; the
 //                                                   softmax modes use q, k raw)
 // The modes without re-weighting are the case p = 1, kappa = 1, beta = 0.
-// Scores are formed exactly as the forward forms them (normalised modes: the
-// rows scaled by 1/max(|x|, 1e-12) and rounded to fp16, products summed in
-// fp32; softmax modes: raw bf16 rows), because at large p the weights are far
-// more sensitive to a mismatch between the saved row constants and the
-// recomputed scores than to the score error itself.
+// Scores are formed exactly as the forward forms them (normalised modes: key
+// rows scaled by 1/max(|x|, 1e-12), query rows by a_i/max(|x|, 1e-12) with
+// a_i = qmul ln i, both rounded to fp16, products summed in fp32 -- the score
+// is then z itself; softmax modes: raw bf16 rows), because at large p the
+// weights are far more sensitive to a mismatch between the saved row
+// constants and the recomputed scores than to the score error itself.
 // A uniform (all-zero re-weighted) row is saved as kappa = 0, beta = 1,
 // W = i: constant weights 1/i and no gradient through its scores.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "lssar_internal.cuh"
+#include "tc_host.cuh"
 
 namespace lssar {
 namespace {
@@ -108,10 +110,11 @@ __device__ __forceinline__ float2 dot_row(const __nv_bfloat16 *x, const float *y
     return make_float2(dot, ss);
 }
 
-// Score of an fp16-rounded normalised row held in shared memory with a bf16
-// row normalised and rounded the same way: (sum_e h(x_e/|x|) y_e, max(|x|, eps)).
+// Score of an fp16-rounded row held in shared memory with a bf16 row
+// normalised, multiplied by xscale and rounded the same way:
+// (sum_e h(x_e xscale / |x|) y_e, max(|x|, eps)).
 template <int D>
-__device__ __forceinline__ float2 dot_row_fp16(const __nv_bfloat16 *x, const float *yh) {
+__device__ __forceinline__ float2 dot_row_fp16(const __nv_bfloat16 *x, const float *yh, float xscale) {
     const uint4 *r = reinterpret_cast<const uint4 *>(x);
     uint4 u[D / 8];
     float ss = 0.f;
@@ -126,7 +129,8 @@ __device__ __forceinline__ float2 dot_row_fp16(const __nv_bfloat16 *x, const flo
             ss = fmaf(f.y, f.y, ss);
         }
     }
-    const float n = fmaxf(sqrtf(ss), 1e-12f), inv = 1.f / n;
+    const float n = fmaxf(sqrtf(ss), 1e-12f);
+    const float inv = (1.f / n) * xscale;
     float dot = 0.f;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 bwd_simt_rows(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
               const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ dout,
               const float4 *__restrict__ stats, __nv_bfloat16 *__restrict__ dq,
-              float2 *__restrict__ rowws, long long rows_total, int L, int p, int mode) {
+              float2 *__restrict__ rowws, long long rows_total, int L, int p, int mode, float qmul) {
     __shared__ float sq[kWarpsPerBlock][D];
     __shared__ float sqh[kWarpsPerBlock][D];
     __shared__ float sdo[kWarpsPerBlock][D];
@@ -179,7 +183,10 @@ bwd_simt_rows(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restri
     }
     qss = warp_sum(qss);
     const float qn = fmaxf(sqrtf(qss), 1e-12f);
-    for (int t = lane; t < D; t += 32) sqh[warp][t] = __half2float(__float2half_rn(sq[warp][t] * (1.f / qn)));
+    // the forward's query operand: q / max(|q|, eps) * qmul ln i, in fp16
+    float qinv = 1.f / qn;
+    qinv *= qmul * logf((float)i);
+    for (int t = lane; t < D; t += 32) sqh[warp][t] = __half2float(__float2half_rn(sq[warp][t] * qinv));
     __syncwarp();
     const float a = score_scale(mode, D, i);
     const float4 st = stats[qrow];
@@ -193,12 +200,12 @@ bwd_simt_rows(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restri
             s = dot_row<D>(kb + (long long)j * D, sq[warp]).x;
             kscale = 1.f;
         } else {
-            const float2 sk = dot_row_fp16<D>(kb + (long long)j * D, sqh[warp]);
-            s = sk.x;
+            const float2 sk = dot_row_fp16<D>(kb + (long long)j * D, sqh[warp], 1.f);
+            s = sk.x;   // z itself
             kscale = 1.f / sk.y;
         }
         float b;
-        phi_and_slope(mode, a * s, st.x, b, slope);
+        phi_and_slope(mode, raw ? a * s : s, st.x, b, slope);
         const float base = fmaxf(b * st.y + st.z, 0.f);
         u = pe == 1 ? (base > 0.f ? 1.f : 0.f) : powi(base, pe - 1);
         w = pe == 1 ? base : u * base;
@@ -259,7 +266,7 @@ bwd_simt_cols(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restri
               const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ dout,
               const float4 *__restrict__ stats, const float2 *__restrict__ rowws,
               __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, long long rows_total,
-              int L, int p, int mode) {
+              int L, int p, int mode, float qmul) {
     __shared__ float sk[kWarpsPerBlock][D];
     __shared__ float skh[kWarpsPerBlock][D];
     __shared__ float sv[kWarpsPerBlock][D];
@@ -299,15 +306,15 @@ bwd_simt_cols(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restri
                 s = dot_row<D>(qb + (long long)r * D, sk[warp]).x;
                 qscale = 1.f;
             } else {
-                const float2 sq = dot_row_fp16<D>(qb + (long long)r * D, skh[warp]);
-                s = sq.x;
+                const float2 sq = dot_row_fp16<D>(qb + (long long)r * D, skh[warp], qmul * logf((float)(r + 1)));
+                s = sq.x;   // z itself
                 qscale = 1.f / sq.y;
             }
             const float a = score_scale(mode, D, i);
             const float4 st = stats[bh * L + r];
             const float2 rw = rowws[bh * L + r];
             float b, slope;
-            phi_and_slope(mode, a * s, st.x, b, slope);
+            phi_and_slope(mode, raw ? a * s : s, st.x, b, slope);
             const float base = fmaxf(b * st.y + st.z, 0.f);
             const float u = pe == 1 ? (base > 0.f ? 1.f : 0.f) : powi(base, pe - 1);
             const float w = pe == 1 ? base : u * base;
@@ -354,13 +361,14 @@ cudaError_t launch(const BwdProblem &pr, void *ws, cudaStream_t stream) {
     const auto *dout = static_cast<const __nv_bfloat16 *>(pr.dout);
     const auto *st = reinterpret_cast<const float4 *>(pr.stats);
     auto *rowws = static_cast<float2 *>(ws);
+    const float qmul = score_qmul(pr.d);
     bwd_simt_rows<D><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(
-        q, k, v, dout, st, static_cast<__nv_bfloat16 *>(pr.dq), rowws, rows, pr.L, pr.p, pr.mode);
+        q, k, v, dout, st, static_cast<__nv_bfloat16 *>(pr.dq), rowws, rows, pr.L, pr.p, pr.mode, qmul);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_simt_cols<D><<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(
         q, k, v, dout, st, rowws, static_cast<__nv_bfloat16 *>(pr.dk), static_cast<__nv_bfloat16 *>(pr.dv),
-        rows, pr.L, pr.p, pr.mode);
+        rows, pr.L, pr.p, pr.mode, qmul);
     return cudaGetLastError();
 }
 

@@ -122,7 +122,11 @@ cudaError_t launch_bwd_tc(const BwdProblem &pr, void *ws, cudaStream_t stream) {
     const void *qs = pr.q, *ks = pr.k;
     CUtensorMapDataType st = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (normalised) {
-        e = launch_normalize_fp16(pr.q, pr.k, base + lay.qh, base + lay.kh, rows, pr.d, counters + 2, stream);
+        // query rows as a_i qh_i in fp16, as the forward writes them (positive
+        // orientation in every mode: the forward's negated sigmoid rows round
+        // to exactly the negated values)
+        e = launch_normalize_fp16(pr.q, pr.k, base + lay.qh, base + lay.kh, rows, pr.d, counters + 2, stream,
+                                  pr.L, score_qmul(pr.d));
         if (e != cudaSuccess) return e;
         qs = base + lay.qh;
         ks = base + lay.kh;

@@ -24,14 +24,18 @@ __device__ unsigned g_error_word;
 
 // q_i / max(|q_i|, 1e-12) and k_j / max(|k_j|, 1e-12) rounded to fp16 (Key
 // design 1 of the notes: rows are L2-normalised before the score product).
-// Each row is handled by D/8 consecutive threads, 8 elements each.
-// Thread 0 also zeroes the attention kernel's work counter.
+// With qmul != 0 query row i (1-based within its head) is also multiplied by
+// qmul * ln i, so that the score product yields z = qmul ln i qh.kh directly
+// (qmul = +-log2(e) ln d: the length scale in log2 units).  Each row is
+// handled by D/8 consecutive threads, 8 elements each.  Thread 0 also zeroes
+// the attention kernel's work counter.
 template <int D>
 __global__ void __launch_bounds__(256) normalize_rows_fp16(const __nv_bfloat16 *__restrict__ q,
                                                            const __nv_bfloat16 *__restrict__ k,
                                                            __half *__restrict__ qh,
                                                            __half *__restrict__ kh,
-                                                           long long rows, unsigned *counter) {
+                                                           long long rows, unsigned *counter, int L,
+                                                           float qmul) {
     constexpr int G = D / 8;
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (tid == 0) *counter = 0u;
@@ -58,7 +62,8 @@ __global__ void __launch_bounds__(256) normalize_rows_fp16(const __nv_bfloat16 *
 #pragma unroll
     for (int o = G / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (!live) return;
-    const float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+    float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
+    if (!is_k && qmul != 0.f) inv *= qmul * logf((float)(rr % L + 1));
     uint4 u;
     __half2 *h = reinterpret_cast<__half2 *>(&u);
 #pragma unroll
@@ -70,7 +75,7 @@ __global__ void __launch_bounds__(256) normalize_rows_fp16(const __nv_bfloat16 *
 }  // namespace
 
 cudaError_t launch_normalize_fp16(const void *q, const void *k, void *qh, void *kh, long long rows,
-                                  int d, unsigned *counter, cudaStream_t stream) {
+                                  int d, unsigned *counter, cudaStream_t stream, int L, float qmul) {
     const long long threads = 2 * rows * (d / 8);
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -79,9 +84,9 @@ cudaError_t launch_normalize_fp16(const void *q, const void *k, void *qh, void *
     auto *qo = static_cast<__half *>(qh);
     auto *ko = static_cast<__half *>(kh);
     if (d == 64)
-        normalize_rows_fp16<64><<<(unsigned)blocks, 256, 0, stream>>>(qb, kb, qo, ko, rows, counter);
+        normalize_rows_fp16<64><<<(unsigned)blocks, 256, 0, stream>>>(qb, kb, qo, ko, rows, counter, L, qmul);
     else
-        normalize_rows_fp16<128><<<(unsigned)blocks, 256, 0, stream>>>(qb, kb, qo, ko, rows, counter);
+        normalize_rows_fp16<128><<<(unsigned)blocks, 256, 0, stream>>>(qb, kb, qo, ko, rows, counter, L, qmul);
     return cudaGetLastError();
 }
 
@@ -251,7 +256,10 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
         const size_t half = qk_bytes(pr);
         __half *qh = reinterpret_cast<__half *>(static_cast<char *>(ws) + kCounterBytes);
         __half *kh = reinterpret_cast<__half *>(static_cast<char *>(ws) + kCounterBytes + half);
-        cudaError_t e = launch_normalize_fp16(pr.q, pr.k, qh, kh, rows, pr.d, counter, stream);
+        // query rows pre-scaled by the length scale (negated for the sigmoid
+        // normaliser, whose kernel registers hold -z)
+        const float qmul = (pr.mode == kSigmoidRw ? -1.f : 1.f) * score_qmul(pr.d);
+        cudaError_t e = launch_normalize_fp16(pr.q, pr.k, qh, kh, rows, pr.d, counter, stream, pr.L, qmul);
         if (e != cudaSuccess) return e;
         qsrc = qh;
         ksrc = kh;

@@ -5,7 +5,10 @@
 // scaled dot-product formula in its Background section), for row i (1-based)
 // and keys j <= i of one head:
 //   LSSA/LSSAR scores  z_ij = log2(e) * ln d * ln i * qh_i . kh_j, with qh, kh
-//                      the L2-normalised rows (prepared in fp16 by a prologue)
+//                      the L2-normalised rows prepared in fp16 by a prologue
+//                      that also multiplies query row i by log2(e) ln d ln i
+//                      (by its negative for the sigmoid normaliser), so that
+//                      the score product yields z itself
 //   softmax scores     z_ij = log2(e) / sqrt(d) * q_i . k_j (raw bf16 rows)
 //   sp2(z) = log2(1 + 2^z) = softplus(x) / ln 2  for z = x log2 e
 //   pass 1 (LSSAR):    S1_i = sum_j sp2(z_ij),  m_i = max_j z_ij, the softplus sum
@@ -250,16 +253,20 @@ struct RowConst {
     bool uniform;  // re-weighted row read as all-zero (prefix mean)
 };
 
-// Scores of one 32-column chunk to z = a * s in place; on the diagonal tile
-// the columns above row t become -inf (+inf for the sigmoid mode, whose
-// registers hold -z).
+// Scores of one 32-column chunk to z in place: z = a * s for the softmax
+// normalisers (raw q, k); the normalised modes' query rows already carry the
+// length scale (the prologue writes a_i qh_i in fp16), so their S is z and
+// only the diagonal tile is touched.  On the diagonal tile the columns above
+// row t become -inf (+inf for the sigmoid mode, whose registers hold -z).
 template <int MODE, bool DIAG>
 __device__ __forceinline__ void to_z(uint32_t (&r)[32], int col0, int t, float a) {
     constexpr float kMasked = MODE == kSigmoidRw ? INFINITY : -INFINITY;
+    constexpr bool kScaled = uses_normalised_qk(MODE);
+    if (kScaled && !DIAG) return;
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
-        float2 z = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                              make_float2(a, a));
+        float2 z = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+        if (!kScaled) z = __fmul2_rn(z, make_float2(a, a));
         if (DIAG) {
             if (col0 + j > t) z.x = kMasked;
             if (col0 + j + 1 > t) z.y = kMasked;
