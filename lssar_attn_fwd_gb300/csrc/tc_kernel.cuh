@@ -129,8 +129,11 @@ template <int D>
 struct Cfg {
     static constexpr int kTileBytes = kBM * D * 2;       // one Q, K or V tile
     static constexpr int kStages = D == 64 ? 8 : 4;      // ring stages
+    // Q-tile pair buffers: two at d = 64, so that the next item's Q tiles load
+    // while the current item runs (at d = 128 shared memory holds one)
+    static constexpr int kQBufs = D == 64 ? 2 : 1;
     static constexpr int kQOff = 0;
-    static constexpr int kRingOff = 2 * kTileBytes;
+    static constexpr int kRingOff = kQBufs * 2 * kTileBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
     static constexpr int kBarBytes = 8192;
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
@@ -141,7 +144,7 @@ constexpr uint32_t kItemConsumers = 1 + 4 * kBM;   // MMA thread + four warpgrou
 constexpr uint32_t kTileThreads = 2 * kBM;           // the two warpgroups of one Q tile
 
 struct __align__(8) Barriers {
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];
     uint64_t s_full[2], s_free[2], o_full[2], o_free[2], p_full[2], p_free[2];
     uint64_t kv_full[8], kv_empty[8];
     uint64_t item_full[kItemQ], item_empty[kItemQ];
@@ -399,8 +402,10 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     constexpr uint32_t kIdescPV = ptx::idesc_f16(true, kBM, D, false, true);
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(ptx::smem_u32(&bars->q_full), 1);
-        ptx::mbar_init(ptx::smem_u32(&bars->q_empty), 1);
+        for (int b = 0; b < C::kQBufs; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&bars->q_full[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->q_empty[b]), 1);
+        }
         for (int w = 0; w < 2; ++w) {
             ptx::mbar_init(ptx::smem_u32(&bars->s_full[w]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->s_free[w]), kTileThreads);
@@ -492,16 +497,18 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const int qa = 2 * m, qb = 2 * m + 1;
                 const bool vb = qb < prm.n_qtiles;
                 const int nk = vb ? qb + 1 : qa + 1;
-                if (q_cnt > 0 && !wait_bar(ptx::smem_u32(&bars->q_empty), (q_cnt - 1) & 1, bars,
-                                           prm.err, kErrQEmpty))
+                const uint32_t qbuf = q_cnt % C::kQBufs, quse = q_cnt / C::kQBufs;
+                if (quse > 0 && !wait_bar(ptx::smem_u32(&bars->q_empty[qbuf]), (quse - 1) & 1, bars,
+                                          prm.err, kErrQEmpty))
                     break;
-                const uint32_t qf = ptx::smem_u32(&bars->q_full);
+                const uint32_t qf = ptx::smem_u32(&bars->q_full[qbuf]);
+                uint8_t *qdst = sQ + qbuf * 2 * TB;
                 ptx::mbar_arrive_expect_tx(qf, (vb ? 2 : 1) * TB);
 #pragma unroll
                 for (int b = 0; b < D / 64; ++b) {
-                    ptx::tma_load_3d(ptx::smem_u32(sQ + b * 16384), &tmQ, qf, b * 64, qa * kBM, bh);
+                    ptx::tma_load_3d(ptx::smem_u32(qdst + b * 16384), &tmQ, qf, b * 64, qa * kBM, bh);
                     if (vb)
-                        ptx::tma_load_3d(ptx::smem_u32(sQ + TB + b * 16384), &tmQ, qf, b * 64,
+                        ptx::tma_load_3d(ptx::smem_u32(qdst + TB + b * 16384), &tmQ, qf, b * 64,
                                          qb * kBM, bh);
                 }
                 ++q_cnt;
@@ -517,8 +524,9 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             // wait (bounded) until the last stages and Q tiles issued have landed.
             for (uint32_t i = ring_idx > (uint32_t)NS ? ring_idx - NS : 0; i < ring_idx; ++i)
                 wait_bar(ptx::smem_u32(&bars->kv_full[i % NS]), (i / NS) & 1, bars, prm.err, kErrDrain, false);
-            if (q_cnt > 0)
-                wait_bar(ptx::smem_u32(&bars->q_full), (q_cnt - 1) & 1, bars, prm.err, kErrDrain, false);
+            for (uint32_t i = q_cnt > (uint32_t)C::kQBufs ? q_cnt - C::kQBufs : 0; i < q_cnt; ++i)
+                wait_bar(ptx::smem_u32(&bars->q_full[i % C::kQBufs]), (i / C::kQBufs) & 1, bars, prm.err,
+                         kErrDrain, false);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -552,8 +560,9 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const uint64_t desc_q0 = ptx::smem_desc_sw128(ptx::smem_u32(sQ), kKmajorLbo, kKmajorSbo);
             const uint64_t desc_k0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kKmajorLbo, kKmajorSbo);
             const uint64_t desc_v0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kVLbo, kVSbo);
+            uint32_t qoff = 0;   // byte offset of the current item's Q buffer
             auto issue_s = [&](int w, uint32_t kslot) {
-                const uint64_t dq = desc_q0 + (uint64_t)((w * TB) >> 4);
+                const uint64_t dq = desc_q0 + (uint64_t)((qoff + w * TB) >> 4);
                 const uint64_t dk = desc_k0 + (uint64_t)((kslot * TB) >> 4);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
@@ -583,9 +592,12 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const bool vb = qb < prm.n_qtiles;
                 const int n_w[2] = {qa + 1, vb ? qb + 1 : 0};
                 const int nk = vb ? qb + 1 : qa + 1;
-                if (!(ok = wait_bar(ptx::smem_u32(&bars->q_full), q_cnt & 1, bars, prm.err, kErrQFull)))
+                const uint32_t qbuf = q_cnt % C::kQBufs;
+                if (!(ok = wait_bar(ptx::smem_u32(&bars->q_full[qbuf]), (q_cnt / C::kQBufs) & 1, bars, prm.err,
+                                    kErrQFull)))
                     break;
                 ++q_cnt;
+                qoff = qbuf * 2 * TB;
                 ptx::tc_fence_after();
                 uint32_t slot;
                 if (kTwoPass) {
@@ -664,7 +676,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         if (has_next) ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[kslot]));
                     }
                 }
-                ptx::mma_commit(ptx::smem_u32(&bars->q_empty));
+                ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qbuf]));
             }
         }
         __syncwarp();
