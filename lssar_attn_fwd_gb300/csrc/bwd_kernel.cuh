@@ -701,12 +701,13 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 // ---------------- column pass: key row arow, query tiles at..n_tiles-1
                 const float R = __uint_as_float(prm.rmax[bh]);
                 const float invR = R > 0.f ? 1.f / R : 0.f;
-                // rec: this tile's query records, field-major ([field][128 queries])
-                auto col_tile = [&](const uint32_t (&rs)[32], const uint32_t (&rd)[32], const float *rec,
-                                    uint32_t (&w1)[16], uint32_t (&w2)[16], auto diag) {
+                // rec: this tile's query records, field-major ([field][128 queries]).
+                // A warpgroup's 32 columns go in two 16-column halves.
+                auto col_half = [&](const uint32_t (&rs)[16], const uint32_t (&rd)[16], const float *rec,
+                                    int col0, uint32_t (&w1)[8], uint32_t (&w2)[8], auto diag) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        const int q0 = 32 * g + c;
+                    for (int c = 0; c < 16; c += 4) {
+                        const int q0 = col0 + c;
                         float4 f[8];
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
@@ -742,18 +743,68 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                     }
                 };
                 for (int qt = p0; qt < p1; ++qt) {
-                    uint32_t rs[32], rd[32];
-                    if (!(ok = load_scores(rs, rd))) break;
+                    if (!(ok = wait_warp(s_full, sf_phase, kErrSFull))) break;
+                    sf_phase ^= 1;
+                    ptx::tc_fence_after();
                     // this tile's query records (the stage's bulk copy has landed:
                     // its mbarrier phase is complete once S was issued)
                     const uint32_t slot = ring_idx % NS, use = ring_idx / NS;
                     ++ring_idx;
                     if (!(ok = wait_warp(ptx::smem_u32(&bars->ring_full[slot]), use & 1, kErrRingFull))) break;
                     const float *rec = reinterpret_cast<const float *>(ring + slot * C::kStageBytes + 2 * TB);
-                    uint32_t w1[16], w2[16];
-                    if (qt == at) col_tile(rs, rd, rec, w1, w2, Diag());
-                    else col_tile(rs, rd, rec, w1, w2, OffDiag());
-                    if (!(ok = store_a(w1, w2))) break;
+                    if constexpr (T::kAlias) {
+                        // d = 128 (A over S / dP, released by the accumulation):
+                        // one 16-column half in registers at a time
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t rs[16], rd[16];
+                            ptx::tmem_ld16(s_col + 16 * half, rs);
+                            ptx::tmem_ld16(dp_col + 16 * half, rd);
+                            ptx::tmem_ld_wait();
+                            ptx::reg_fence(rs);
+                            ptx::reg_fence(rd);
+                            uint32_t w1[8], w2[8];
+                            if (qt == at) col_half(rs, rd, rec, 32 * g + 16 * half, w1, w2, Diag());
+                            else col_half(rs, rd, rec, 32 * g + 16 * half, w1, w2, OffDiag());
+                            // these words overwrite S / dP columns of the first half,
+                            // which are already in registers
+                            ptx::tmem_st8(a1_col + 8 * half, w1);
+                            ptx::tmem_st8(a2_col + 8 * half, w2);
+                        }
+                    } else {
+                        // d = 64: one 16-column half in registers at a time; S / dP
+                        // are released once the second half is loaded
+                        uint32_t w1[2][8], w2[2][8];
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t rsh[16], rdh[16];
+                            ptx::tmem_ld16(s_col + 16 * half, rsh);
+                            ptx::tmem_ld16(dp_col + 16 * half, rdh);
+                            ptx::tmem_ld_wait();
+                            ptx::reg_fence(rsh);
+                            ptx::reg_fence(rdh);
+                            if (half == 1) {
+                                ptx::tc_fence_before();
+                                ptx::mbar_arrive(s_free);
+                            }
+                            if (qt == at) col_half(rsh, rdh, rec, 32 * g + 16 * half, w1[half], w2[half], Diag());
+                            else col_half(rsh, rdh, rec, 32 * g + 16 * half, w1[half], w2[half], OffDiag());
+                        }
+                        if (a_pending) {   // the previous tile's A words have been read
+                            if (!(ok = wait_warp(a_free, af_phase, kErrAFree))) break;
+                            af_phase ^= 1;
+                            ptx::tc_fence_after();
+                        }
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            ptx::tmem_st8(a1_col + 8 * half, w1[half]);
+                            ptx::tmem_st8(a2_col + 8 * half, w2[half]);
+                        }
+                    }
+                    ptx::tmem_st_wait();
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(a_full);
+                    a_pending = true;
                 }
                 if (!ok) break;
                 // epilogue: dkh = R * Acc1, dv = Acc2
