@@ -852,14 +852,30 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if constexpr (kSepP) {
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(s_free);   // the next S MMA may start now
+                    // both chunks' weights first: the previous P.V MMA reads P
+                    // meanwhile, and the wait for it comes just before the stores
+                    uint32_t pk0[16], pk1[16];
+                    if (kt == qt) to_z<MODE, true>(r0, 64 * h, t, rc.a);
+                    else to_z<MODE, false>(r0, 64 * h, t, rc.a);
+                    weights_z<MODE, PK>(r0, rc, p_row, acc2[0], pk0);
+                    if (kt == qt) to_z<MODE, true>(r1, 64 * h + 32, t, rc.a);
+                    else to_z<MODE, false>(r1, 64 * h + 32, t, rc.a);
+                    weights_z<MODE, PK>(r1, rc, p_row, acc2[1], pk1);
                     if (p_pending) {
                         if (!(ok = wait_warp(p_free, pf_phase, kErrPFree))) break;
                         pf_phase ^= 1;
                         ptx::tc_fence_after();
                     }
+                    ptx::tmem_st16(p_col, pk0);
+                    ptx::tmem_st16(p_col + 16, pk1);
+                    ptx::tmem_st_wait();
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(p_full);   // P(kt) is in TMEM
+                    p_pending = true;
+                    continue;
                 }
-                // each 16-word half of this thread's P row is stored as soon as it
-                // is ready (d = 128: over S columns already loaded above)
+                // d = 128: each 16-word half of this thread's P row is stored over S
+                // columns already loaded above as soon as it is ready
                 {
                     uint32_t pk[16];
                     if (kt == qt) to_z<MODE, true>(r0, 64 * h, t, rc.a);
@@ -876,12 +892,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 }
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
-                if constexpr (kSepP) {
-                    ptx::mbar_arrive(p_full);   // P(kt) is in TMEM
-                    p_pending = true;
-                } else {
-                    ptx::mbar_arrive(s_free);   // P(kt) is in TMEM over the S columns
-                }
+                ptx::mbar_arrive(s_free);   // P(kt) is in TMEM over the S columns
             }
             if (!ok) break;
             bars->x_s2[w][h][t] = (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
