@@ -19,19 +19,10 @@ cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CU
     constexpr int smem = Cfg<D>::kSmemBytes;
     static PerDeviceOnce once;
     cudaError_t e = per_device_once(once, nullptr, [&](int &) {
-        // With the register split enabled, the re-allocation must fit in what
-        // the launch provides, or the increase would never be granted.
-        cudaFuncAttributes attr;
-        cudaError_t r = cudaFuncGetAttributes(&attr, kern);
-        if (r != cudaSuccess) return r;
-        const long long launch_regs = (long long)attr.numRegs * kThreads;
-        const long long split_regs = 32LL * kScoreWarp0 * kRegsCtl + 2LL * kTileThreads * kRegsScore;
-        if (kRegSplit && (split_regs > launch_regs || attr.numRegs > kRegsScore))
-            return cudaErrorInvalidConfiguration;
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, prm);
+    kern<<<grid, Cfg<D>::kThreads, smem, stream>>>(mq, mk, mv, prm);
     return cudaGetLastError();
 }
 

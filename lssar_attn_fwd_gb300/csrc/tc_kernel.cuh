@@ -33,22 +33,27 @@
 //                         for this mode (scale -a, mask +inf) so 2^-z needs no negation.
 //   out_i = (sum_j w_ij v_j) / (sum_j w_ij)
 //
-// Structure (one persistent CTA per SM, 640 threads = 5 warpgroups):
+// Structure (one persistent CTA per SM; 608 threads = 19 warps at d = 64, 576 at d = 128):
 //   warp 0      TMA producer: Q tiles once per work item, then K (pass 1) and
 //               K, V (pass 2) tiles through an NS-stage shared-memory ring.
-//   warp 1      TMEM owner and single-thread tcgen05.mma issuer.
-//   warps 2-3   idle (they complete warpgroup 0, which gives registers away)
-//   warps 4-19  four score warpgroups g = 0..3: Q tile w = g & 1 of the pair,
+//   warp 1      TMEM owner and tcgen05.mma issuer: for Q tile 0 of the pair at
+//               d = 64, for both tiles at d = 128.
+//   warp 18     (d = 64) tcgen05.mma issuer for Q tile 1.  Each issuer runs its
+//               tile's chain of waits, MMAs and commits on its own, so the two
+//               chains overlap; both walk the whole K/V ring and each releases
+//               every stage.
+//   warps 2-17  four score warpgroups g = 0..3: Q tile w = g & 1 of the pair,
 //               column half h = g >> 1 of its 128-key S tile.  Thread t of a
 //               warpgroup owns query row t (TMEM lane t, lane quarter = warp % 4)
 //               and keys [64h, 64h+64) of every tile: it reads S from TMEM,
 //               computes statistics / weights, writes its 32 words of P (bf16
-//               pairs) back over the first half of its own S columns, and stores
-//               its half of the output row.  Each SM sub-partition therefore runs
-//               four math warps.  The two halves of a row combine their partial
-//               sums and maxima once per item through shared memory.
-// Registers: warpgroup 0 drops to kRegsCtl per thread, the score warpgroups
-// raise theirs to kRegsScore (setmaxnreg).
+//               pairs) to TMEM, and stores its half of the output row.  Each SM
+//               sub-partition therefore runs four math warps.  The two halves of
+//               a row combine their partial sums and maxima once per item
+//               through shared memory.
+// The control warps run their loops warp-wide (one elected lane issues each
+// copy, MMA and commit).  Eighteen or nineteen warps put five on some SM
+// sub-partitions, which caps the registers at 96 per thread.
 // d = 64: P has TMEM columns of its own, so a warpgroup releases S as soon as
 // it has loaded it and the next S MMA overlaps the weight computation; P is
 // double-checked free by a commit after each P.V MMA.  d = 128: TMEM is full
@@ -81,11 +86,8 @@ namespace tc {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr bool kRegSplit = false;                  // setmaxnreg re-allocation
-constexpr int kThreads = kRegSplit ? 640 : 576;
-constexpr int kScoreWarp0 = kRegSplit ? 4 : 2;     // first score warp
-constexpr int kRegsCtl = 24;     // registers per thread of warpgroup 0 after the split
-constexpr int kRegsScore = 112;  // registers per thread of the score warpgroups
+constexpr int kScoreWarp0 = 2;    // first score warp (warps 2-17)
+constexpr int kMmaWarp1 = 18;     // second MMA issuer, when there are two
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a stuck wait gives up after 2 s
 
 // Error codes written to the device error word (first failure wins).
@@ -137,10 +139,15 @@ struct Cfg {
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
     static constexpr int kBarBytes = 8192;
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
+    // MMA-issuing warps: one per Q tile at d = 64 (P in columns of its own);
+    // at d = 128, where P is written over S, one warp orders both tiles' MMAs.
+    static constexpr int kMmaWarps = D == 64 ? 2 : 1;
+    static constexpr int kThreads = 576 + 32 * (kMmaWarps - 1);
 };
 
 constexpr int kItemQ = 4;                     // depth of the work-item queue
-constexpr uint32_t kItemConsumers = 1 + 4 * kBM;   // MMA thread + four warpgroups
+// work-item queue consumers: the MMA warps (one arrival each) and four warpgroups
+__host__ __device__ constexpr uint32_t item_consumers(int mma_warps) { return mma_warps + 4 * kBM; }
 constexpr uint32_t kTileThreads = 2 * kBM;           // the two warpgroups of one Q tile
 
 struct __align__(8) Barriers {
@@ -377,7 +384,7 @@ __device__ __forceinline__ void weights_z(const uint32_t (&r)[32], const RowCons
 }
 
 template <int D, int MODE, int PK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
 lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const Params prm) {
     using C = Cfg<D>;
@@ -404,7 +411,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int b = 0; b < C::kQBufs; ++b) {
             ptx::mbar_init(ptx::smem_u32(&bars->q_full[b]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->q_empty[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->q_empty[b]), C::kMmaWarps);   // one commit per MMA warp
         }
         for (int w = 0; w < 2; ++w) {
             ptx::mbar_init(ptx::smem_u32(&bars->s_full[w]), 1);
@@ -416,11 +423,11 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->kv_empty[s]), C::kMmaWarps);   // one commit per MMA warp
         }
         for (int s = 0; s < kItemQ; ++s) {
             ptx::mbar_init(ptx::smem_u32(&bars->item_full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->item_empty[s]), kItemConsumers);
+            ptx::mbar_init(ptx::smem_u32(&bars->item_empty[s]), item_consumers(C::kMmaWarps));
         }
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
@@ -434,12 +441,6 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    if constexpr (kRegSplit) {
-        if (warp < kScoreWarp0)
-            ptx::setmaxnreg_dec<kRegsCtl>();
-        else
-            ptx::setmaxnreg_inc<kRegsScore>();
-    }
 
     const int BH = prm.BH;
     auto decode = [&](int item, int &bh, int &m) {
@@ -447,35 +448,45 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         bh = item % BH;
     };
     // Consumer side of the work-item queue: returns false on a timed-out wait.
-    auto next_item = [&](uint32_t &qi, int &item) -> bool {
+    auto next_item = [&](uint32_t &qi, int &item, bool arrive = true) -> bool {
         const uint32_t s = qi % kItemQ, use = qi / kItemQ;
         ++qi;
         if (!wait_bar(ptx::smem_u32(&bars->item_full[s]), use & 1, bars, prm.err, kErrItem))
             return false;
         item = *(volatile int *)&bars->item_q[s];
-        ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[s]));
+        if (arrive) ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[s]));
         return true;
+    };
+    // A wait taken by every lane of a control warp; the outcome is made
+    // warp-uniform so that the warp's control flow never diverges.
+    auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned code, bool honour_abort = true) -> bool {
+        return __all_sync(0xffffffffu, wait_bar(bar, parity, bars, prm.err, code, honour_abort));
     };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            ptx::prefetch_tensormap(&tmQ);
-            ptx::prefetch_tensormap(&tmK);
-            ptx::prefetch_tensormap(&tmV);
+        // (the whole warp runs the loop; one elected lane issues the copies)
+        {
+            if (ptx::elect_one()) {
+                ptx::prefetch_tensormap(&tmQ);
+                ptx::prefetch_tensormap(&tmK);
+                ptx::prefetch_tensormap(&tmV);
+            }
             uint32_t ring_idx = 0, q_cnt = 0, qi = 0;
             bool ok = true;
             auto push = [&](const CUtensorMap *map, int tile, int bh) -> bool {
                 const uint32_t s = ring_idx % NS, use = ring_idx / NS;
-                if (use > 0 && !wait_bar(ptx::smem_u32(&bars->kv_empty[s]), (use - 1) & 1, bars,
-                                         prm.err, kErrKvEmpty))
+                if (use > 0 && !wait_all(ptx::smem_u32(&bars->kv_empty[s]), (use - 1) & 1, kErrKvEmpty))
                     return false;
                 const uint32_t full = ptx::smem_u32(&bars->kv_full[s]);
-                ptx::mbar_arrive_expect_tx(full, TB);
+                if (ptx::elect_one()) {
+                    ptx::mbar_arrive_expect_tx(full, TB);
 #pragma unroll
-                for (int b = 0; b < D / 64; ++b)
-                    ptx::tma_load_3d(ptx::smem_u32(ring + s * TB + b * 16384), map, full, b * 64,
-                                     tile * kBN, bh);
+                    for (int b = 0; b < D / 64; ++b)
+                        ptx::tma_load_3d(ptx::smem_u32(ring + s * TB + b * 16384), map, full, b * 64,
+                                         tile * kBN, bh);
+                }
+                __syncwarp();
                 ++ring_idx;
                 return true;
             };
@@ -483,13 +494,19 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 // claim and publish the next work item
                 const uint32_t s = qi % kItemQ, use = qi / kItemQ;
                 const int fixed = qi < 2 ? prm.first_items[blockIdx.x][qi] : -1;
-                const int item = fixed >= 0 ? fixed : (int)(prm.tail_base + atomicAdd(prm.counter, 1u));
+                int item = fixed;
+                if (fixed < 0) {
+                    if (lane == 0) item = (int)(prm.tail_base + atomicAdd(prm.counter, 1u));
+                    item = __shfl_sync(0xffffffffu, item, 0);
+                }
                 ++qi;
-                if (use > 0 && !wait_bar(ptx::smem_u32(&bars->item_empty[s]), (use - 1) & 1, bars,
-                                         prm.err, kErrItem))
+                if (use > 0 && !wait_all(ptx::smem_u32(&bars->item_empty[s]), (use - 1) & 1, kErrItem))
                     break;
-                *(volatile int *)&bars->item_q[s] = item;
-                ptx::mbar_arrive(ptx::smem_u32(&bars->item_full[s]));
+                if (lane == 0) {
+                    *(volatile int *)&bars->item_q[s] = item;
+                    ptx::mbar_arrive(ptx::smem_u32(&bars->item_full[s]));
+                }
+                __syncwarp();
                 if (item >= prm.n_items) break;
 
                 int bh, m;
@@ -498,19 +515,21 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const bool vb = qb < prm.n_qtiles;
                 const int nk = vb ? qb + 1 : qa + 1;
                 const uint32_t qbuf = q_cnt % C::kQBufs, quse = q_cnt / C::kQBufs;
-                if (quse > 0 && !wait_bar(ptx::smem_u32(&bars->q_empty[qbuf]), (quse - 1) & 1, bars,
-                                          prm.err, kErrQEmpty))
+                if (quse > 0 && !wait_all(ptx::smem_u32(&bars->q_empty[qbuf]), (quse - 1) & 1, kErrQEmpty))
                     break;
                 const uint32_t qf = ptx::smem_u32(&bars->q_full[qbuf]);
                 uint8_t *qdst = sQ + qbuf * 2 * TB;
-                ptx::mbar_arrive_expect_tx(qf, (vb ? 2 : 1) * TB);
+                if (ptx::elect_one()) {
+                    ptx::mbar_arrive_expect_tx(qf, (vb ? 2 : 1) * TB);
 #pragma unroll
-                for (int b = 0; b < D / 64; ++b) {
-                    ptx::tma_load_3d(ptx::smem_u32(qdst + b * 16384), &tmQ, qf, b * 64, qa * kBM, bh);
-                    if (vb)
-                        ptx::tma_load_3d(ptx::smem_u32(qdst + TB + b * 16384), &tmQ, qf, b * 64,
-                                         qb * kBM, bh);
+                    for (int b = 0; b < D / 64; ++b) {
+                        ptx::tma_load_3d(ptx::smem_u32(qdst + b * 16384), &tmQ, qf, b * 64, qa * kBM, bh);
+                        if (vb)
+                            ptx::tma_load_3d(ptx::smem_u32(qdst + TB + b * 16384), &tmQ, qf, b * 64,
+                                             qb * kBM, bh);
+                    }
                 }
+                __syncwarp();
                 ++q_cnt;
                 if (kTwoPass)
                     for (int kt = 0; ok && kt < nk; ++kt) ok = push(&tmK, kt, bh);
@@ -529,53 +548,84 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                          kErrDrain, false);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t ring_idx = 0, q_cnt = 0, qi = 0;
-            uint32_t sf_phase[2] = {0, 0}, of_phase[2] = {0, 0}, pf_phase[2] = {0, 0};
-            bool s_pending[2] = {false, false}, o_pending[2] = {false, false};
-            bool ok = true;
-            auto acquire = [&](uint32_t &slot) -> bool {
-                slot = ring_idx % NS;
-                const uint32_t use = ring_idx / NS;
-                ++ring_idx;
-                if (!wait_bar(ptx::smem_u32(&bars->kv_full[slot]), use & 1, bars, prm.err,
-                              kErrKvFull))
-                    return false;
-                ptx::tc_fence_after();
-                return true;
-            };
-            auto touch_s = [&](int w) -> bool {
-                if (!s_pending[w]) return true;
-                if (!wait_bar(ptx::smem_u32(&bars->s_free[w]), sf_phase[w], bars, prm.err, kErrSFree))
-                    return false;
-                sf_phase[w] ^= 1;
-                s_pending[w] = false;
-                ptx::tc_fence_after();
-                return true;
-            };
-            // Descriptors are built once; a K step moves the start address field
-            // (16-byte units, bits 0-13), which never carries for these offsets.
-            const uint64_t desc_q0 = ptx::smem_desc_sw128(ptx::smem_u32(sQ), kKmajorLbo, kKmajorSbo);
-            const uint64_t desc_k0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kKmajorLbo, kKmajorSbo);
-            const uint64_t desc_v0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kVLbo, kVSbo);
-            uint32_t qoff = 0;   // byte offset of the current item's Q buffer
-            auto issue_s = [&](int w, uint32_t kslot) {
-                const uint64_t dq = desc_q0 + (uint64_t)((qoff + w * TB) >> 4);
-                const uint64_t dk = desc_k0 + (uint64_t)((kslot * TB) >> 4);
+    } else if (warp == 1 || (C::kMmaWarps == 2 && warp == kMmaWarp1)) {
+        // ------------------------------------------------------------ MMA issuers
+        // d = 64: warp 1 issues for Q tile 0 of each pair and warp kMmaWarp1 for
+        // tile 1, so that the two tiles' chains of waits and issues overlap;
+        // d = 128: warp 1 issues for both tiles (NT = 2).  The whole warp runs
+        // the loop; one elected lane issues the MMAs and commits.  Every MMA
+        // warp walks the producer's whole stage sequence and commits every
+        // stage's release (a stage is free after one commit per MMA warp).
+        constexpr int NT = C::kMmaWarps == 2 ? 1 : 2;   // Q tiles per MMA warp
+        const int wbase = warp == 1 ? 0 : 1;
+        auto tile = [&](int t) { return NT == 2 ? t : wbase; };
+        uint32_t ring_idx = 0, q_cnt = 0, qi = 0;
+        uint32_t sf_phase[NT], of_phase[NT], pf_phase[NT];
+        bool s_pending[NT], o_pending[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            sf_phase[t] = of_phase[t] = pf_phase[t] = 0;
+            s_pending[t] = o_pending[t] = false;
+        }
+        bool ok = true;
+        auto acquire = [&](uint32_t &slot) -> bool {
+            slot = ring_idx % NS;
+            const uint32_t use = ring_idx / NS;
+            ++ring_idx;
+            if (!wait_all(ptx::smem_u32(&bars->kv_full[slot]), use & 1, kErrKvFull)) return false;
+            ptx::tc_fence_after();
+            return true;
+        };
+        // S of tile t may be overwritten once its warpgroups have released it
+        auto touch_s = [&](int t) -> bool {
+            if (!s_pending[t]) return true;
+            if (!wait_all(ptx::smem_u32(&bars->s_free[tile(t)]), sf_phase[t], kErrSFree)) return false;
+            sf_phase[t] ^= 1;
+            s_pending[t] = false;
+            ptx::tc_fence_after();
+            return true;
+        };
+        auto wait_o_free = [&](int t) -> bool {
+            if (!o_pending[t]) return true;
+            if (!wait_all(ptx::smem_u32(&bars->o_free[tile(t)]), of_phase[t], kErrOFree)) return false;
+            of_phase[t] ^= 1;
+            o_pending[t] = false;
+            ptx::tc_fence_after();
+            return true;
+        };
+        auto commit = [&](uint64_t *bar) {
+            const uint32_t b = ptx::smem_u32(bar);
+            if (ptx::elect_one()) ptx::mma_commit(b);
+            __syncwarp();
+        };
+        // Descriptors are built once; a K step moves the start address field
+        // (16-byte units, bits 0-13), which never carries for these offsets.
+        const uint64_t desc_q0 = ptx::smem_desc_sw128(ptx::smem_u32(sQ), kKmajorLbo, kKmajorSbo);
+        const uint64_t desc_k0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kKmajorLbo, kKmajorSbo);
+        const uint64_t desc_v0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kVLbo, kVSbo);
+        uint32_t qoff = 0;   // byte offset of the current item's Q buffer
+        auto issue_s = [&](int t, uint32_t kslot) {
+            const int w = tile(t);
+            const uint64_t dq = desc_q0 + (uint64_t)((qoff + w * TB) >> 4);
+            const uint64_t dk = desc_k0 + (uint64_t)((kslot * TB) >> 4);
+            const uint32_t full = ptx::smem_u32(&bars->s_full[w]);
+            if (ptx::elect_one()) {
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = ((k / 4) * 16384 + (k % 4) * 32) >> 4;
                     ptx::mma_ss(tmem + w * kBN, dq + off, dk + off, kIdescS, k > 0);
                 }
-                ptx::mma_commit(ptx::smem_u32(&bars->s_full[w]));
-                s_pending[w] = true;
-            };
-            auto issue_pv = [&](int w, uint32_t vslot, bool accumulate) {
-                const uint64_t dv = desc_v0 + (uint64_t)((vslot * TB) >> 4);
-                // P words of keys 16k..16k+15: d = 64, 8k of P_w; d = 128, words
-                // (k%4)*8 of the S column half k/4
+                ptx::mma_commit(full);
+            }
+            __syncwarp();
+            s_pending[t] = true;
+        };
+        auto issue_pv = [&](int t, uint32_t vslot, bool accumulate) {
+            const int w = tile(t);
+            const uint64_t dv = desc_v0 + (uint64_t)((vslot * TB) >> 4);
+            // P words of keys 16k..16k+15: d = 64, 8k of P_w; d = 128, words
+            // (k%4)*8 of the S column half k/4
+            if (ptx::elect_one()) {
 #pragma unroll
                 for (int k = 0; k < kBN / 16; ++k)
                     ptx::mma_ts(tmem + kOCol + w * D,
@@ -583,101 +633,87 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                       : tmem + w * kBN + (k / 4) * 64 + (k % 4) * 8,
                                 dv + (uint64_t)((k * 2048) >> 4), kIdescPV,
                                 (accumulate || k > 0) ? 1u : 0u);
-            };
-            int item;
-            while (ok && (ok = next_item(qi, item)) && item < prm.n_items) {
-                int bh, m;
-                decode(item, bh, m);
-                const int qa = 2 * m, qb = 2 * m + 1;
-                const bool vb = qb < prm.n_qtiles;
-                const int n_w[2] = {qa + 1, vb ? qb + 1 : 0};
-                const int nk = vb ? qb + 1 : qa + 1;
-                const uint32_t qbuf = q_cnt % C::kQBufs;
-                if (!(ok = wait_bar(ptx::smem_u32(&bars->q_full[qbuf]), (q_cnt / C::kQBufs) & 1, bars, prm.err,
-                                    kErrQFull)))
-                    break;
-                ++q_cnt;
-                qoff = qbuf * 2 * TB;
-                ptx::tc_fence_after();
-                uint32_t slot;
-                if (kTwoPass) {
-                    for (int kt = 0; ok && kt < nk; ++kt) {
-                        if (!(ok = acquire(slot))) break;
-                        for (int w = 0; w < 2 && ok; ++w)
-                            if (kt < n_w[w]) {
-                                if (!(ok = touch_s(w))) break;
-                                issue_s(w, slot);
-                            }
-                        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[slot]));
-                    }
-                }
-                if (!ok || !(ok = acquire(slot))) break;
-                for (int w = 0; w < 2 && ok; ++w)
-                    if (n_w[w] > 0) {
-                        if (!(ok = touch_s(w))) break;
-                        issue_s(w, slot);
-                    }
-                ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[slot]));
-                auto wait_o_free = [&](int w) -> bool {
-                    if (!o_pending[w]) return true;
-                    if (!wait_bar(ptx::smem_u32(&bars->o_free[w]), of_phase[w], bars, prm.err,
-                                  kErrOFree))
-                        return false;
-                    of_phase[w] ^= 1;
-                    o_pending[w] = false;
-                    ptx::tc_fence_after();
-                    return true;
-                };
-                for (int kt = 0; ok && kt < nk; ++kt) {
-                    const bool has_next = kt + 1 < nk;
-                    uint32_t kslot = 0, vslot;
-                    if (has_next && !(ok = acquire(kslot))) break;
-                    if constexpr (kSepP) {
-                        // next scores as soon as each warpgroup has loaded S(kt)
-                        for (int w = 0; w < 2 && ok; ++w)
-                            if (kt + 1 < n_w[w]) {
-                                if (!(ok = touch_s(w))) break;
-                                issue_s(w, kslot);
-                            }
-                        if (!ok) break;
-                        if (has_next) ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[kslot]));
-                        if (!(ok = acquire(vslot))) break;
-                        for (int w = 0; w < 2 && ok; ++w) {
-                            if (kt >= n_w[w]) continue;
-                            if (!(ok = wait_bar(ptx::smem_u32(&bars->p_full[w]), pf_phase[w], bars,
-                                                prm.err, kErrPFull)))
-                                break;
-                            pf_phase[w] ^= 1;
-                            ptx::tc_fence_after();
-                            if (kt == 0 && !(ok = wait_o_free(w))) break;
-                            issue_pv(w, vslot, kt > 0);
-                            ptx::mma_commit(ptx::smem_u32(&bars->p_free[w]));
-                            if (kt + 1 == n_w[w]) {
-                                ptx::mma_commit(ptx::smem_u32(&bars->o_full[w]));
-                                o_pending[w] = true;
-                            }
-                        }
-                        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[vslot]));
-                    } else {
-                        if (!(ok = acquire(vslot))) break;
-                        for (int w = 0; w < 2 && ok; ++w) {
-                            if (kt >= n_w[w]) continue;
-                            if (!(ok = touch_s(w))) break;   // P_w(kt) is in TMEM
-                            if (kt == 0 && !(ok = wait_o_free(w))) break;
-                            issue_pv(w, vslot, kt > 0);
-                            if (kt + 1 < n_w[w]) {
-                                issue_s(w, kslot);
-                            } else {
-                                ptx::mma_commit(ptx::smem_u32(&bars->o_full[w]));
-                                o_pending[w] = true;
-                            }
-                        }
-                        ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[vslot]));
-                        if (has_next) ptx::mma_commit(ptx::smem_u32(&bars->kv_empty[kslot]));
-                    }
-                }
-                ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qbuf]));
             }
+            __syncwarp();
+        };
+        int item;
+        while (ok && (ok = __all_sync(0xffffffffu, next_item(qi, item, lane == 0))) && item < prm.n_items) {
+            int bh, m;
+            decode(item, bh, m);
+            const int qa = 2 * m, qb = 2 * m + 1;
+            const bool vb = qb < prm.n_qtiles;
+            const int n_w[2] = {qa + 1, vb ? qb + 1 : 0};   // K tiles of each Q tile
+            const int nk = vb ? qb + 1 : qa + 1;            // K tiles the producer streams
+            const uint32_t qbuf = q_cnt % C::kQBufs;
+            if (!(ok = wait_all(ptx::smem_u32(&bars->q_full[qbuf]), (q_cnt / C::kQBufs) & 1, kErrQFull)))
+                break;
+            ++q_cnt;
+            qoff = qbuf * 2 * TB;
+            ptx::tc_fence_after();
+            uint32_t slot;
+            if (kTwoPass) {
+                for (int kt = 0; ok && kt < nk; ++kt) {
+                    if (!(ok = acquire(slot))) break;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t)
+                        if (ok && kt < n_w[tile(t)] && (ok = touch_s(t))) issue_s(t, slot);
+                    commit(&bars->kv_empty[slot]);
+                }
+            }
+            if (!ok || !(ok = acquire(slot))) break;
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                if (ok && n_w[tile(t)] > 0 && (ok = touch_s(t))) issue_s(t, slot);
+            commit(&bars->kv_empty[slot]);
+            for (int kt = 0; ok && kt < nk; ++kt) {
+                const bool has_next = kt + 1 < nk;
+                uint32_t kslot = 0, vslot;
+                if (has_next && !(ok = acquire(kslot))) break;
+                if constexpr (kSepP) {
+                    // next scores as soon as the warpgroups have loaded S(kt)
+#pragma unroll
+                    for (int t = 0; t < NT; ++t)
+                        if (ok && kt + 1 < n_w[tile(t)] && (ok = touch_s(t))) issue_s(t, kslot);
+                    if (!ok) break;
+                    if (has_next) commit(&bars->kv_empty[kslot]);
+                    if (!(ok = acquire(vslot))) break;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        const int w = tile(t);
+                        if (!ok || kt >= n_w[w]) continue;
+                        if (!(ok = wait_all(ptx::smem_u32(&bars->p_full[w]), pf_phase[t], kErrPFull))) continue;
+                        pf_phase[t] ^= 1;
+                        ptx::tc_fence_after();
+                        if (kt == 0 && !(ok = wait_o_free(t))) continue;
+                        issue_pv(t, vslot, kt > 0);
+                        commit(&bars->p_free[w]);
+                        if (kt + 1 == n_w[w]) {
+                            commit(&bars->o_full[w]);
+                            o_pending[t] = true;
+                        }
+                    }
+                    commit(&bars->kv_empty[vslot]);
+                } else {
+                    if (!(ok = acquire(vslot))) break;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        const int w = tile(t);
+                        if (!ok || kt >= n_w[w]) continue;
+                        if (!(ok = touch_s(t))) continue;   // P_w(kt) is in TMEM
+                        if (kt == 0 && !(ok = wait_o_free(t))) continue;
+                        issue_pv(t, vslot, kt > 0);
+                        if (kt + 1 < n_w[w]) {
+                            issue_s(t, kslot);
+                        } else {
+                            commit(&bars->o_full[w]);
+                            o_pending[t] = true;
+                        }
+                    }
+                    commit(&bars->kv_empty[vslot]);
+                    if (has_next) commit(&bars->kv_empty[kslot]);
+                }
+            }
+            commit(&bars->q_empty[qbuf]);
         }
         __syncwarp();
     } else {
