@@ -222,6 +222,23 @@ __device__ __forceinline__ float2 sp2x2_direct(float2 z) {
     return make_float2(ptx::lg2(v.x), ptx::lg2(v.y));
 }
 
+// sp2 with log2(1 + u), u = 2^-|z| in [0, 1], from a polynomial on the FMA
+// pipe instead of the MUFU lg2: log2(1 + u) ~= u (c1 + u (c2 + ... + u c6)),
+// coefficients fitted by minimax (Lawson-weighted least squares) on [0, 1]
+// with the constant term fixed at 0, so that a masked column (u = 0,
+// z = -inf) still gives exactly 0; largest error 2.2e-6 in fp32 Horner
+// arithmetic.
+__device__ __forceinline__ float2 sp2x2_poly(float2 z) {
+    const float2 u = make_float2(ptx::ex2(-fabsf(z.x)), ptx::ex2(-fabsf(z.y)));
+    float2 h = __ffma2_rn(u, make_float2(-0.02645743452012539f, -0.02645743452012539f),
+                          make_float2(0.12345144152641296f, 0.12345144152641296f));
+    h = __ffma2_rn(h, u, make_float2(-0.279538094997406f, -0.279538094997406f));
+    h = __ffma2_rn(h, u, make_float2(0.458270788192749f, 0.458270788192749f));
+    h = __ffma2_rn(h, u, make_float2(-0.7182819247245789f, -0.7182819247245789f));
+    h = __ffma2_rn(h, u, make_float2(1.442553162574768f, 1.442553162574768f));
+    return __ffma2_rn(h, u, make_float2(fmaxf(z.x, 0.f), fmaxf(z.y, 0.f)));
+}
+
 __device__ __forceinline__ float sp2(float z) {
     return ptx::lg2(1.f + ptx::ex2(z));
 }
@@ -350,6 +367,13 @@ __device__ __forceinline__ void softmax_tile_stats(const uint32_t (&r0)[32], con
     m_run = mn;
 }
 
+// Pairs of each 16-pair chunk whose LSSAR softplus takes the polynomial log2
+// (spread evenly over the chunk), to share the pass-2 work between the MUFU
+// and FMA pipes.  The longer power chains (p = 15, runtime p) leave the FMA
+// pipe less room.  Measured at the 8K shape, kernel TFLOP/s for 0/3/5/7 of 16:
+// p = 15 607.6/626.5/622.0/619.0, p = 3 632.8/645.4/678.0/668.1.
+__host__ __device__ constexpr int poly_pairs(int pk) { return (pk == 15 || pk == 0) ? 3 : 5; }
+
 // Pass-2 weights of one chunk of z, summed into acc and packed to 16 bf16x2.
 template <int MODE, int PK>
 __device__ __forceinline__ void weights_z(const uint32_t (&r)[32], const RowConst &rc, int p,
@@ -366,7 +390,9 @@ __device__ __forceinline__ void weights_z(const uint32_t (&r)[32], const RowCons
         } else {
             float2 phi;   // the normaliser's nonnegative value (up to a per-row factor)
             if constexpr (MODE == kLssar) {
-                phi = sp2x2_direct(z);
+                constexpr int kPoly = poly_pairs(PK);
+                if (((j / 2) * kPoly) % 16 < kPoly) phi = sp2x2_poly(z);
+                else phi = sp2x2_direct(z);
             } else if constexpr (MODE == kSoftmaxRw) {
                 const float2 e = __fadd2_rn(z, make_float2(-rc.m, -rc.m));
                 phi = make_float2(ptx::ex2(e.x), ptx::ex2(e.y));
