@@ -311,72 +311,90 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
             p1 = prm.n_tiles;
         }
     };
-    auto next_item = [&](uint32_t &qi, int &item) -> bool {
+    auto next_item = [&](uint32_t &qi, int &item, bool arrive = true) -> bool {
         const uint32_t s = qi % kItemQ, use = qi / kItemQ;
         ++qi;
         if (!wait_bar(ptx::smem_u32(&bars->item_full[s]), use & 1, bars, prm.err, kErrItem))
             return false;
         item = *(volatile int *)&bars->item_q[s];
-        ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[s]));
+        if (arrive) ptx::mbar_arrive(ptx::smem_u32(&bars->item_empty[s]));
         return true;
+    };
+    // A wait taken by every lane of a control warp; the outcome is made
+    // warp-uniform so that the warp's control flow never diverges.
+    auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned code) -> bool {
+        return __all_sync(0xffffffffu, wait_bar(bar, parity, bars, prm.err, code));
     };
     constexpr int kPasses = kRow ? 2 : 1;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            ptx::prefetch_tensormap(&tmX1);
-            ptx::prefetch_tensormap(&tmX2);
-            ptx::prefetch_tensormap(&tmY1);
-            ptx::prefetch_tensormap(&tmY2);
+        // (the whole warp runs the loop; one elected lane issues the copies)
+        {
+            if (ptx::elect_one()) {
+                ptx::prefetch_tensormap(&tmX1);
+                ptx::prefetch_tensormap(&tmX2);
+                ptx::prefetch_tensormap(&tmY1);
+                ptx::prefetch_tensormap(&tmY2);
+            }
             uint32_t ring_idx = 0, x_cnt = 0, qi = 0;
             bool ok = true;
             while (ok) {
                 const uint32_t s = qi % kItemQ, use = qi / kItemQ;
-                const int item = qi == 0 ? (int)blockIdx.x
-                                         : (int)(gridDim.x + atomicAdd(prm.counter, 1u));
+                int item = (int)blockIdx.x;
+                if (qi > 0) {
+                    if (lane == 0) item = (int)(gridDim.x + atomicAdd(prm.counter, 1u));
+                    item = __shfl_sync(0xffffffffu, item, 0);
+                }
                 ++qi;
-                if (use > 0 && !wait_bar(ptx::smem_u32(&bars->item_empty[s]), (use - 1) & 1, bars,
-                                         prm.err, kErrItem))
+                if (use > 0 && !wait_all(ptx::smem_u32(&bars->item_empty[s]), (use - 1) & 1, kErrItem))
                     break;
-                *(volatile int *)&bars->item_q[s] = item;
-                ptx::mbar_arrive(ptx::smem_u32(&bars->item_full[s]));
+                if (lane == 0) {
+                    *(volatile int *)&bars->item_q[s] = item;
+                    ptx::mbar_arrive(ptx::smem_u32(&bars->item_full[s]));
+                }
+                __syncwarp();
                 if (item >= prm.n_items) break;
                 int bh, at, p0, p1;
                 decode(item, bh, at, p0, p1);
-                if (x_cnt > 0 && !wait_bar(ptx::smem_u32(&bars->x_empty), (x_cnt - 1) & 1, bars,
-                                           prm.err, kErrXEmpty))
+                if (x_cnt > 0 && !wait_all(ptx::smem_u32(&bars->x_empty), (x_cnt - 1) & 1, kErrXEmpty))
                     break;
                 const uint32_t xf = ptx::smem_u32(&bars->x_full);
-                ptx::mbar_arrive_expect_tx(xf, 2 * TB);
+                if (ptx::elect_one()) {
+                    ptx::mbar_arrive_expect_tx(xf, 2 * TB);
 #pragma unroll
-                for (int b = 0; b < D / 64; ++b) {
-                    ptx::tma_load_3d(ptx::smem_u32(sX + b * 16384), &tmX1, xf, b * 64, at * kBM, bh);
-                    ptx::tma_load_3d(ptx::smem_u32(sX + TB + b * 16384), &tmX2, xf, b * 64, at * kBM, bh);
+                    for (int b = 0; b < D / 64; ++b) {
+                        ptx::tma_load_3d(ptx::smem_u32(sX + b * 16384), &tmX1, xf, b * 64, at * kBM, bh);
+                        ptx::tma_load_3d(ptx::smem_u32(sX + TB + b * 16384), &tmX2, xf, b * 64, at * kBM, bh);
+                    }
                 }
+                __syncwarp();
                 ++x_cnt;
                 for (int pass = 0; ok && pass < kPasses; ++pass) {
                     for (int t = p0; ok && t < p1; ++t) {
                         const uint32_t st = ring_idx % NS, su = ring_idx / NS;
-                        if (su > 0 && !wait_bar(ptx::smem_u32(&bars->ring_empty[st]), (su - 1) & 1, bars,
-                                                prm.err, kErrRingEmpty)) {
+                        if (su > 0 && !wait_all(ptx::smem_u32(&bars->ring_empty[st]), (su - 1) & 1,
+                                                kErrRingEmpty)) {
                             ok = false;
                             break;
                         }
                         uint8_t *stage = ring + st * C::kStageBytes;
                         const uint32_t full = ptx::smem_u32(&bars->ring_full[st]);
-                        ptx::mbar_arrive_expect_tx(full, 2 * TB + (kRow ? 0 : C::kConstBytes));
+                        if (ptx::elect_one()) {
+                            ptx::mbar_arrive_expect_tx(full, 2 * TB + (kRow ? 0 : C::kConstBytes));
 #pragma unroll
-                        for (int b = 0; b < D / 64; ++b) {
-                            ptx::tma_load_3d(ptx::smem_u32(stage + b * 16384), &tmY1, full, b * 64,
-                                             t * kBN, bh);
-                            ptx::tma_load_3d(ptx::smem_u32(stage + TB + b * 16384), &tmY2, full, b * 64,
-                                             t * kBN, bh);
+                            for (int b = 0; b < D / 64; ++b) {
+                                ptx::tma_load_3d(ptx::smem_u32(stage + b * 16384), &tmY1, full, b * 64,
+                                                 t * kBN, bh);
+                                ptx::tma_load_3d(ptx::smem_u32(stage + TB + b * 16384), &tmY2, full, b * 64,
+                                                 t * kBN, bh);
+                            }
+                            if (!kRow)
+                                ptx::bulk_load(ptx::smem_u32(stage + 2 * TB),
+                                               prm.rowc + ((size_t)bh * prm.n_tiles + t) * 8 * kBN,
+                                               C::kConstBytes, full);
                         }
-                        if (!kRow)
-                            ptx::bulk_load(ptx::smem_u32(stage + 2 * TB),
-                                           prm.rowc + ((size_t)bh * prm.n_tiles + t) * 8 * kBN,
-                                           C::kConstBytes, full);
+                        __syncwarp();
                         ++ring_idx;
                     }
                 }
@@ -391,7 +409,9 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // (the whole warp runs the loop; one elected lane issues the MMAs and
+        // commits)
+        {
             uint32_t ring_idx = 0, x_cnt = 0, qi = 0;
             uint32_t sf_phase = 0, af_phase = 0, accf_phase = 0;
             bool s_pending = false, acc_pending = false;
@@ -400,15 +420,18 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 slot = ring_idx % NS;
                 const uint32_t use = ring_idx / NS;
                 ++ring_idx;
-                if (!wait_bar(ptx::smem_u32(&bars->ring_full[slot]), use & 1, bars, prm.err, kErrRingFull))
-                    return false;
+                if (!wait_all(ptx::smem_u32(&bars->ring_full[slot]), use & 1, kErrRingFull)) return false;
                 ptx::tc_fence_after();
                 return true;
             };
+            auto commit = [&](uint64_t *bar) {
+                const uint32_t b = ptx::smem_u32(bar);
+                if (ptx::elect_one()) ptx::mma_commit(b);
+                __syncwarp();
+            };
             auto touch_s = [&]() -> bool {
                 if (!s_pending) return true;
-                if (!wait_bar(ptx::smem_u32(&bars->s_free), sf_phase, bars, prm.err, kErrSFree))
-                    return false;
+                if (!wait_all(ptx::smem_u32(&bars->s_free), sf_phase, kErrSFree)) return false;
                 sf_phase ^= 1;
                 s_pending = false;
                 ptx::tc_fence_after();
@@ -422,17 +445,21 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
             auto issue_scores = [&](uint32_t slot) {
                 const uint64_t y1 = dy0 + (uint64_t)((slot * C::kStageBytes) >> 4);
                 const uint64_t y2 = dy0 + (uint64_t)((slot * C::kStageBytes + TB) >> 4);
+                const uint32_t full = ptx::smem_u32(&bars->s_full);
+                if (ptx::elect_one()) {
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = ((k / 4) * 16384 + (k % 4) * 32) >> 4;
-                    ptx::mma_ss(tmem + T::kS, dx1 + off, y1 + off, kIdescS, k > 0);
-                }
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = ((k / 4) * 16384 + (k % 4) * 32) >> 4;
+                        ptx::mma_ss(tmem + T::kS, dx1 + off, y1 + off, kIdescS, k > 0);
+                    }
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = ((k / 4) * 16384 + (k % 4) * 32) >> 4;
-                    ptx::mma_ss(tmem + T::kDP, dx2 + off, y2 + off, kIdescDP, k > 0);
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t off = ((k / 4) * 16384 + (k % 4) * 32) >> 4;
+                        ptx::mma_ss(tmem + T::kDP, dx2 + off, y2 + off, kIdescDP, k > 0);
+                    }
+                    ptx::mma_commit(full);
                 }
-                ptx::mma_commit(ptx::smem_u32(&bars->s_full));
+                __syncwarp();
                 // with the A operands over S / dP the warpgroups signal a_full only
                 s_pending = !T::kAlias;
             };
@@ -443,24 +470,26 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
             auto issue_acc = [&](uint32_t slot, bool accumulate) {
                 const uint64_t m1 = dm0 + (uint64_t)((slot * C::kStageBytes) >> 4);
                 const uint64_t m2 = dm0 + (uint64_t)((slot * C::kStageBytes + TB) >> 4);
-#pragma unroll
-                for (int k = 0; k < kBN / 16; ++k)
-                    ptx::mma_ts(tmem + T::kAcc1, a_addr(T::kA1, k), m1 + (uint64_t)((k * 2048) >> 4),
-                                kIdescA1, (accumulate || k > 0) ? 1u : 0u);
-                if (!kRow) {
+                if (ptx::elect_one()) {
 #pragma unroll
                     for (int k = 0; k < kBN / 16; ++k)
-                        ptx::mma_ts(tmem + T::kAcc2, a_addr(T::kA2, k), m2 + (uint64_t)((k * 2048) >> 4),
-                                    kIdescA2, (accumulate || k > 0) ? 1u : 0u);
+                        ptx::mma_ts(tmem + T::kAcc1, a_addr(T::kA1, k), m1 + (uint64_t)((k * 2048) >> 4),
+                                    kIdescA1, (accumulate || k > 0) ? 1u : 0u);
+                    if (!kRow) {
+#pragma unroll
+                        for (int k = 0; k < kBN / 16; ++k)
+                            ptx::mma_ts(tmem + T::kAcc2, a_addr(T::kA2, k), m2 + (uint64_t)((k * 2048) >> 4),
+                                        kIdescA2, (accumulate || k > 0) ? 1u : 0u);
+                    }
                 }
+                __syncwarp();
             };
             int item;
-            while (ok && (ok = next_item(qi, item)) && item < prm.n_items) {
+            while (ok && (ok = __all_sync(0xffffffffu, next_item(qi, item, lane == 0))) && item < prm.n_items) {
                 int bh, at, p0, p1;
                 decode(item, bh, at, p0, p1);
                 const int n = p1 - p0;
-                if (!(ok = wait_bar(ptx::smem_u32(&bars->x_full), x_cnt & 1, bars, prm.err, kErrXFull)))
-                    break;
+                if (!(ok = wait_all(ptx::smem_u32(&bars->x_full), x_cnt & 1, kErrXFull))) break;
                 ++x_cnt;
                 ptx::tc_fence_after();
                 uint32_t slot;
@@ -469,7 +498,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                     for (int t = 0; ok && t < n; ++t) {
                         if (!(ok = acquire(slot)) || !(ok = touch_s())) break;
                         issue_scores(slot);
-                        ptx::mma_commit(ptx::smem_u32(&bars->ring_empty[slot]));
+                        commit(&bars->ring_empty[slot]);
                     }
                     if (!ok) break;
                 }
@@ -485,21 +514,18 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                         if (!(ok = acquire(nxt)) || !(ok = touch_s())) break;
                         issue_scores(nxt);
                     }
-                    if (!(ok = wait_bar(ptx::smem_u32(&bars->a_full), af_phase, bars, prm.err, kErrAFull)))
-                        break;
+                    if (!(ok = wait_all(ptx::smem_u32(&bars->a_full), af_phase, kErrAFull))) break;
                     af_phase ^= 1;
                     ptx::tc_fence_after();
                     if (t == 0 && acc_pending) {
-                        if (!(ok = wait_bar(ptx::smem_u32(&bars->acc_free), accf_phase, bars, prm.err,
-                                            kErrAccFree)))
-                            break;
+                        if (!(ok = wait_all(ptx::smem_u32(&bars->acc_free), accf_phase, kErrAccFree))) break;
                         accf_phase ^= 1;
                         acc_pending = false;
                         ptx::tc_fence_after();
                     }
                     issue_acc(cur, t > 0);
-                    ptx::mma_commit(ptx::smem_u32(&bars->a_free));
-                    ptx::mma_commit(ptx::smem_u32(&bars->ring_empty[cur]));
+                    commit(&bars->a_free);
+                    commit(&bars->ring_empty[cur]);
                     if (T::kAlias && has_next) {
                         // A was written over S / dP: the next scores follow the
                         // accumulation in issue order
@@ -509,8 +535,8 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                     cur = nxt;
                 }
                 if (!ok) break;
-                ptx::mma_commit(ptx::smem_u32(&bars->acc_full));
-                ptx::mma_commit(ptx::smem_u32(&bars->x_empty));
+                commit(&bars->acc_full);
+                commit(&bars->x_empty);
                 acc_pending = true;
             }
         }
