@@ -66,19 +66,28 @@ def peaks():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def kernel_source_sha():
+    """Hash of the attention kernel's device sources (the kernel template and the
+    headers only it uses), to tell whether recorded counters still apply."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("tc_kernel.cuh", "softplus_poly.cuh"):
+        with open(os.path.join(ROOT, "lssar_attn_fwd_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(workload, mode, p):
     """dram read+write bytes per launch of the attention kernel from the
     committed ncu summary, if it was taken on the current kernel source."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        src = os.path.join(ROOT, "lssar_attn_fwd_gb300", "csrc", "tc_kernel.cuh")
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        h = kernel_source_sha()
         key = f"{workload}:{mode}:{p}"
         ent = rec.get(key)
-        if ent and ent.get("tc_kernel_sha") == h:
+        if ent and ent.get("kernel_src_sha") == h:
             return float(ent["dram_bytes_per_launch"])
     except Exception:
         pass

@@ -79,6 +79,7 @@
 #include <cuda_fp16.h>
 
 #include "lssar_internal.cuh"
+#include "softplus_poly.cuh"
 #include "tc_ptx.cuh"
 
 namespace lssar {
@@ -222,23 +223,6 @@ __device__ __forceinline__ float2 sp2x2_direct(float2 z) {
     return make_float2(ptx::lg2(v.x), ptx::lg2(v.y));
 }
 
-// sp2 with log2(1 + u), u = 2^-|z| in [0, 1], from a polynomial on the FMA
-// pipe instead of the MUFU lg2: log2(1 + u) ~= u (c1 + u (c2 + ... + u c6)),
-// coefficients fitted by minimax (Lawson-weighted least squares) on [0, 1]
-// with the constant term fixed at 0, so that a masked column (u = 0,
-// z = -inf) still gives exactly 0; largest error 2.2e-6 in fp32 Horner
-// arithmetic.
-__device__ __forceinline__ float2 sp2x2_poly(float2 z) {
-    const float2 u = make_float2(ptx::ex2(-fabsf(z.x)), ptx::ex2(-fabsf(z.y)));
-    float2 h = __ffma2_rn(u, make_float2(-0.02645743452012539f, -0.02645743452012539f),
-                          make_float2(0.12345144152641296f, 0.12345144152641296f));
-    h = __ffma2_rn(h, u, make_float2(-0.279538094997406f, -0.279538094997406f));
-    h = __ffma2_rn(h, u, make_float2(0.458270788192749f, 0.458270788192749f));
-    h = __ffma2_rn(h, u, make_float2(-0.7182819247245789f, -0.7182819247245789f));
-    h = __ffma2_rn(h, u, make_float2(1.442553162574768f, 1.442553162574768f));
-    return __ffma2_rn(h, u, make_float2(fmaxf(z.x, 0.f), fmaxf(z.y, 0.f)));
-}
-
 __device__ __forceinline__ float sp2(float z) {
     return ptx::lg2(1.f + ptx::ex2(z));
 }
@@ -289,17 +273,18 @@ template <int MODE, bool DIAG>
 __device__ __forceinline__ void to_z(uint32_t (&r)[32], int col0, int t, float a) {
     constexpr float kMasked = MODE == kSigmoidRw ? INFINITY : -INFINITY;
     constexpr bool kScaled = uses_normalised_qk(MODE);
-    if (kScaled && !DIAG) return;
+    if constexpr (!kScaled || DIAG) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-        float2 z = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-        if (!kScaled) z = __fmul2_rn(z, make_float2(a, a));
-        if (DIAG) {
-            if (col0 + j > t) z.x = kMasked;
-            if (col0 + j + 1 > t) z.y = kMasked;
+        for (int j = 0; j < 32; j += 2) {
+            float2 z = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+            if (!kScaled) z = __fmul2_rn(z, make_float2(a, a));
+            if (DIAG) {
+                if (col0 + j > t) z.x = kMasked;
+                if (col0 + j + 1 > t) z.y = kMasked;
+            }
+            r[j] = __float_as_uint(z.x);
+            r[j + 1] = __float_as_uint(z.y);
         }
-        r[j] = __float_as_uint(z.x);
-        r[j + 1] = __float_as_uint(z.y);
     }
 }
 
@@ -390,8 +375,7 @@ __device__ __forceinline__ void weights_z(const uint32_t (&r)[32], const RowCons
         } else {
             float2 phi;   // the normaliser's nonnegative value (up to a per-row factor)
             if constexpr (MODE == kLssar) {
-                constexpr int kPoly = poly_pairs(PK);
-                if (((j / 2) * kPoly) % 16 < kPoly) phi = sp2x2_poly(z);
+                if (poly_pair(j / 2, poly_pairs(PK))) phi = sp2x2_poly(z);
                 else phi = sp2x2_direct(z);
             } else if constexpr (MODE == kSoftmaxRw) {
                 const float2 e = __fadd2_rn(z, make_float2(-rc.m, -rc.m));
