@@ -160,8 +160,17 @@ int lssar_attn_bwd_simt(const void *q, const void *k, const void *v, const void 
  *   k_cache : [B, H, L, d] bfloat16, device (keys 1..L, the new one last).
  *   v_cache : [B, H, L, d] bfloat16, device.
  *   out     : [B, H, d] bfloat16, device, written.
- * Bound by HBM: K and V are read once (scores are kept in a float scratch of
- * 4*B*H*L bytes between the passes).  Same errors as lssar_attn_fwd.
+ * Bound by HBM: K and V are read once.  Each head's cache is cut into up to
+ * 16 chunks of at most 4096 keys that form one thread-block cluster: the
+ * chunks' statistics and partial outputs meet in distributed shared memory
+ * and the scores stay in shared memory, so a step is one launch that touches
+ * no other global memory.  Longer caches (over 65536 keys per head) take a
+ * cooperative launch with a grid barrier, or three launches when that grid
+ * cannot be resident at once; those paths keep scores and partials in a
+ * float scratch of about 4*B*H*L bytes from the library's pool.  The
+ * environment variable LSSAR_DECODE_PATH=grid (or split) makes a call skip
+ * the cluster path (or use the three launches), to test those paths at small
+ * sizes.  Same errors as lssar_attn_fwd.
  */
 int lssar_attn_decode(const void *q, const void *k_cache, const void *v_cache, void *out,
                       int B, int H, int L, int d, int p, int mode, cudaStream_t stream);

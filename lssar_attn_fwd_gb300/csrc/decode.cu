@@ -21,6 +21,9 @@
 // stages are requested before the CTA's prologue, so the copy engine runs
 // ahead of the arithmetic.  Every wait on the ring is bounded: after 2 s the
 // kernel records a code in the device error word and leaves its loop.
+#include <cstdlib>
+#include <cstring>
+
 #include <cuda_bf16.h>
 
 #include "lssar_internal.cuh"
@@ -318,16 +321,24 @@ dec_scores(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict_
 // The head's row constants from its chunks' (max, sum of phi), then the
 // weights of this chunk's n scores z[] into w[] (w may be z: in place).
 // Every thread of the CTA takes part.
-__device__ void chunk_weights(const float2 *__restrict__ part_head, int nch, int L, int mode, int p,
-                              const float *z, float *w, int n) {
-    // read through L2: other CTAs of the same launch may have written them
+// The head's row maximum and normaliser sum from its chunks' (max, sum of
+// phi) pairs, which `stat(u)` returns for chunk u (the softmax normalisers'
+// sums are relative to each chunk's own max).
+template <typename Stat>
+__device__ float2 head_stats(Stat stat, int nch, int mode) {
     float m = -INFINITY;
-    for (int u = 0; u < nch; ++u) m = fmaxf(m, __ldcg(part_head + u).x);
+    for (int u = 0; u < nch; ++u) m = fmaxf(m, stat(u).x);
     float s1 = 0.f;
     for (int u = 0; u < nch; ++u) {
-        const float2 pu = __ldcg(part_head + u);
+        const float2 pu = stat(u);
         s1 += (mode == kSoftmax || mode == kSoftmaxRw) ? pu.y * exp2f(pu.x - m) : pu.y;
     }
+    return make_float2(m, s1);
+}
+
+// The chunk's weights w_j from its scores z_j and the head's statistics.
+__device__ void weights_from_stats(float2 hs, int L, int mode, int p, const float *z, float *w, int n) {
+    const float m = hs.x, s1 = hs.y;
     float kappa = 0.f, beta = 0.f;
     bool uniform = false;
     if (is_reweight(mode)) {
@@ -350,6 +361,13 @@ __device__ void chunk_weights(const float2 *__restrict__ part_head, int nch, int
         else wj = uniform ? 1.f : powi(fmaxf(phi(mode, zj, m) * kappa + beta, 0.f), p);
         w[jj] = wj;
     }
+}
+
+__device__ void chunk_weights(const float2 *__restrict__ part_head, int nch, int L, int mode, int p,
+                              const float *z, float *w, int n) {
+    // read through L2: other CTAs of the same launch may have written them
+    const float2 hs = head_stats([&](int u) { return __ldcg(part_head + u); }, nch, mode);
+    weights_from_stats(hs, L, mode, p, z, w, n);
 }
 
 template <int D>
@@ -530,6 +548,119 @@ dec_fused(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__
     }
 }
 
+// The whole step as one launch with one thread-block cluster per head (the
+// cluster's CTAs are the head's chunks, rank = chunk): phase A streams the
+// chunk's keys and keeps the scores in shared memory; the chunks' (max, sum
+// of phi) meet through distributed shared memory at a cluster barrier; phase
+// B forms the weights and streams the values (the producer has already
+// fetched the first value stages); rank 0 sums the chunks' partial outputs
+// from its partners' shared memory.  Heads never wait on one another, and no
+// global memory beyond q, k, v and out is touched.  Every thread of every CTA
+// reaches each cluster barrier (no path returns early; a timed-out copy wait
+// only sets the error word and the abort flag).
+template <int D>
+__global__ void __launch_bounds__(kDecBlock, kDecCtasPerSm)
+dec_cluster(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+            const __nv_bfloat16 *__restrict__ v, int L, int chunk, int mode, int p,
+            __nv_bfloat16 *__restrict__ out, unsigned *err, int withhold_copies) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    DecSmem *sm = reinterpret_cast<DecSmem *>(dsm);
+    __shared__ float qs[D];
+    __shared__ float accs[kDecWarps][D];
+    __shared__ float2 stat;          // this chunk's (max, sum of phi)
+    __shared__ float opart[D + 1];   // this chunk's sum_j w_j v_j and sum_j w_j
+    const int bh = blockIdx.y, c = blockIdx.x, nch = gridDim.x;
+    const int j0 = c * chunk, j1 = min(L, j0 + chunk);
+    const int n = j1 - j0;
+    const bool raw = !uses_normalised_qk(mode);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool producer = warp == kDecWarps;
+    const Ring<D> rk{sm, k + ((size_t)bh * L + j0) * D, n, err, 0};
+    const int n_st = rk.stages();
+    const Ring<D> rv{sm, v + ((size_t)bh * L + j0) * D, n, err, n_st};
+    init_ring(sm);
+    // withhold_copies (self-test of the failure path only): the producer
+    // issues nothing, so every consumer wait runs into its bound
+    const int n_issue = withhold_copies ? 0 : n_st;
+    int issued_k = 0, issued_v = 0;
+    if (producer && lane == 0) issued_k = rk.issue_upto(0, min(n_issue, kDecStages));
+    // phase A: scores
+    float qss = 0.f;
+    for (int t = threadIdx.x; t < D; t += kDecBlock) {
+        const float x = __bfloat162float(q[(size_t)bh * D + t]);
+        qs[t] = x;
+        qss += x * x;
+    }
+    qss = block_reduce(qss, false, sm->red);
+    const float log2e = 1.4426950408889634f;
+    const float a = raw ? log2e * rsqrtf((float)D)
+                        : log2e * logf((float)D) * logf((float)L) / fmaxf(sqrtf(qss), 1e-12f);
+    float m = -INFINITY;
+    if (producer) {
+        if (lane == 0) {
+            issued_k = rk.issue_upto(issued_k, n_issue);
+            // the first value stages follow as the consumers free the ring
+            if (issued_k == n_st) issued_v = rv.issue_upto(0, min(n_st, kDecStages));
+        }
+        __syncwarp();
+    } else {
+        m = consume_scores<D>(rk, qs, a, raw, nullptr);
+    }
+    m = block_reduce(m, true, sm->red);   // its barriers also publish the scores
+    float sum = 0.f;
+    for (int jj = threadIdx.x; jj < n; jj += kDecBlock) sum += phi(mode, sm->row[jj], m);
+    sum = block_reduce(sum, false, sm->red);
+    if (threadIdx.x == 0) stat = make_float2(m, sum);
+    ptx::cluster_sync();   // every chunk's statistics are in its CTA's shared memory
+    const uint32_t stat_addr = ptx::smem_u32(&stat);
+    const float2 hs = head_stats(
+        [&](int u) {
+            const uint32_t r = ptx::cluster_map(stat_addr, (uint32_t)u);
+            return make_float2(ptx::ld_cluster_f32(r), ptx::ld_cluster_f32(r + 4));
+        },
+        nch, mode);
+    // phase B: weights in place of the scores, then the values
+    weights_from_stats(hs, L, mode, p, sm->row, sm->row, n);
+    __syncthreads();
+    if (producer) {
+        if (lane == 0) {
+            if (issued_k == n_st) issued_v = rv.issue_upto(issued_v, n_st);
+            // the last kDecStages copies of the K-then-V sequence have landed
+            // (earlier ones were consumed, and their slots reused)
+            const int total = issued_k + issued_v;
+            for (int g = max(0, total - kDecStages); g < total; ++g)
+                dec_wait(ptx::smem_u32(&sm->full[g % kDecStages]), (g / kDecStages) & 1, sm, err, kErrDecDrain,
+                         false);
+        }
+        __syncwarp();
+    } else {
+        consume_pv<D>(rv, accs);
+    }
+    float s2 = 0.f;
+    for (int jj = threadIdx.x; jj < n; jj += kDecBlock) s2 += sm->row[jj];
+    s2 = block_reduce(s2, false, sm->red);   // also orders the accs writes before the reads below
+    for (int t = threadIdx.x; t < D; t += kDecBlock) {
+        float r = 0.f;
+        for (int w2 = 0; w2 < kDecWarps; ++w2) r += accs[w2][t];
+        opart[t] = r;
+    }
+    if (threadIdx.x == 0) opart[D] = s2;
+    ptx::cluster_sync();   // every chunk's partial output is in its CTA's shared memory
+    if (c == 0) {
+        const uint32_t op_addr = ptx::smem_u32(opart);
+        for (int t = threadIdx.x; t < D; t += kDecBlock) {
+            float o = 0.f, sw = 0.f;
+            for (int u = 0; u < nch; ++u) {
+                const uint32_t r = ptx::cluster_map(op_addr, (uint32_t)u);
+                o += ptx::ld_cluster_f32(r + 4u * (uint32_t)t);
+                sw += ptx::ld_cluster_f32(r + 4u * D);
+            }
+            out[(size_t)bh * D + t] = __float2bfloat16_rn(o / sw);
+        }
+    }
+    ptx::cluster_sync();   // the partners' shared memory stays in place until rank 0 has read it
+}
+
 // Chunk length: a multiple of 64 rows (whole stages at both head dimensions),
 // at most kDecMaxChunk, and chunks for at most kDecCtasPerSm CTAs per SM (one
 // wave) whenever the heads allow it.
@@ -543,11 +674,70 @@ int choose_chunk(int BH, int L, int sms) {
     return (int)chunk;
 }
 
+constexpr int kDecMaxCluster = 16;   // CTAs per cluster (above 8: non-portable size)
+
+// Chunks per head for the cluster path: about one wave of kDecCtasPerSm CTAs
+// per SM when the heads allow it, at most kDecMaxCluster; 0 when a chunk would
+// exceed kDecMaxChunk rows (the path is then not available).
+int cluster_chunks(int BH, int L, int sms, int *chunk_out) {
+    long long nch = (long long)kDecCtasPerSm * sms / BH;
+    if (nch < 1) nch = 1;
+    if (nch > kDecMaxCluster) nch = kDecMaxCluster;
+    long long chunk = (L + nch - 1) / nch;
+    chunk = ((chunk + 63) / 64) * 64;
+    if (chunk > kDecMaxChunk) return 0;
+    *chunk_out = (int)chunk;
+    return (int)((L + chunk - 1) / chunk);
+}
+
+// Launch of dec_cluster with nch CTAs per cluster, or cudaErrorNotSupported
+// when this device cannot place a cluster of that size (checked once per size).
+template <int D>
+cudaError_t launch_cluster(const DecodeProblem &pr, int BH, int chunk, int nch, unsigned *err, int withhold,
+                           cudaStream_t stream) {
+    const int smem = (int)sizeof(DecSmem);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nch, BH);
+    cfg.blockDim = dim3(kDecBlock);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)nch;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static PerDeviceOnce once[kDecMaxCluster + 1];
+    int fits = 0;
+    cudaError_t e = per_device_once(once[nch], &fits, [&](int &v) {
+        cudaError_t r = cudaFuncSetAttribute(dec_cluster<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (r == cudaSuccess && nch > 8)
+            r = cudaFuncSetAttribute(dec_cluster<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (r != cudaSuccess) return r;
+        int clusters = 0;
+        r = cudaOccupancyMaxActiveClusters(&clusters, dec_cluster<D>, &cfg);
+        if (r != cudaSuccess) {
+            (void)cudaGetLastError();   // a size this device does not support: use the other path
+            clusters = 0;
+        }
+        v = clusters > 0 ? 1 : 0;
+        return cudaSuccess;
+    });
+    if (e != cudaSuccess) return e;
+    if (!fits) return cudaErrorNotSupported;
+    const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
+    const auto *k = static_cast<const __nv_bfloat16 *>(pr.k);
+    const auto *v = static_cast<const __nv_bfloat16 *>(pr.v);
+    auto *o = static_cast<__nv_bfloat16 *>(pr.out);
+    return cudaLaunchKernelEx(&cfg, dec_cluster<D>, q, k, v, pr.L, chunk, pr.mode, pr.p, o, err, withhold);
+}
+
 // One cooperative launch of dec_fused when every CTA of the grid can be
 // resident at once; otherwise the three-kernel sequence.
 template <int D>
 cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, int sms, float *z, float2 *part,
-                     float *opart, unsigned *sync, unsigned *err, int withhold, cudaStream_t stream) {
+                     float *opart, unsigned *sync, unsigned *err, int withhold, bool split, cudaStream_t stream) {
     const int smem = (int)sizeof(DecSmem);
     static PerDeviceOnce once;
     int per_sm = 0;
@@ -558,8 +748,8 @@ cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, int sm
         return r != cudaSuccess ? r : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, dec_fused<D>, kDecBlock, smem);
     });
     if (e != cudaSuccess) return e;
-    if (withhold && (long long)nch * BH > (long long)per_sm * sms) return cudaErrorInvalidConfiguration;
-    if ((long long)nch * BH <= (long long)per_sm * sms) {
+    if (withhold && (split || (long long)nch * BH > (long long)per_sm * sms)) return cudaErrorInvalidConfiguration;
+    if (!split && (long long)nch * BH <= (long long)per_sm * sms) {
         e = cudaMemsetAsync(sync, 0, (size_t)(1 + BH) * sizeof(unsigned), stream);
         if (e != cudaSuccess) return e;
         const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
@@ -611,6 +801,20 @@ cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream
     unsigned *err = nullptr;
     if ((e = error_word_ptr(&err)) != cudaSuccess) return e;
     const int BH = pr.B * pr.H;
+    const int w = withhold_copies ? 1 : 0;
+    // LSSAR_DECODE_PATH=grid | split steers the step away from the cluster
+    // path (grid: the cooperative launch where possible; split: the three
+    // launches), so that tests reach every path at small sizes.
+    const char *force = getenv("LSSAR_DECODE_PATH");
+    const bool no_cluster = force && (strcmp(force, "grid") == 0 || strcmp(force, "split") == 0);
+    const bool split = force && strcmp(force, "split") == 0;
+    int cchunk = 0;
+    const int cnch = no_cluster ? 0 : cluster_chunks(BH, pr.L, sms, &cchunk);
+    if (cnch > 0) {
+        e = pr.d == 64 ? launch_cluster<64>(pr, BH, cchunk, cnch, err, w, stream)
+                       : launch_cluster<128>(pr, BH, cchunk, cnch, err, w, stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
     const int chunk = choose_chunk(BH, pr.L, sms);
     const int nch = (pr.L + chunk - 1) / chunk;
     char *base = static_cast<char *>(ws);
@@ -619,9 +823,8 @@ cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream
     float2 *part = reinterpret_cast<float2 *>(base + lay.part);
     float *opart = reinterpret_cast<float *>(base + lay.opart);
     unsigned *sync = reinterpret_cast<unsigned *>(base + lay.sync);
-    const int w = withhold_copies ? 1 : 0;
-    return pr.d == 64 ? launch_d<64>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, w, stream)
-                      : launch_d<128>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, w, stream);
+    return pr.d == 64 ? launch_d<64>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, w, split, stream)
+                      : launch_d<128>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, w, split, stream);
 }
 
 }  // namespace lssar

@@ -110,6 +110,29 @@ __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- clusters
+
+// Barrier of all threads of all CTAs of the cluster, with release / acquire
+// ordering of their shared-memory writes.  Every thread of every CTA must
+// reach it (it is a hardware barrier, like __syncthreads); the non-.aligned
+// form does not require the warp to be converged there.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Address of the same shared-memory location in the CTA of the given rank.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // True in exactly one lane of the (converged) warp.  The single-thread
 // issue instructions (tcgen05.mma, tcgen05.commit, TMA copies) go under it
 // while the whole warp runs the surrounding control flow, so that addresses,

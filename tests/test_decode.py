@@ -40,7 +40,7 @@ def decode(torch, qb, kb, vb, p, mode):
 
 @pytest.mark.parametrize("L", [1, 2, 3, 4, 255, 1000, 4097, 9000])
 @pytest.mark.parametrize("d", [64, 128])
-def test_decode_matches_last_row(torch_mod, L, d):
+def test_decode_matches_last_row(torch_mod, L, d, decode_path):
     B, H = 2, 3
     qb, kb, vb = make_qkv(B, H, L, d, seed=L + d)
     qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
@@ -76,11 +76,22 @@ def test_decode_equals_prefill_last_row(torch_mod):
     assert np.abs(got - last).max() <= 5e-2
 
 
+@pytest.fixture(params=["cluster", "grid", "split"])
+def decode_path(request, monkeypatch):
+    # cluster: one thread-block cluster per head (the default wherever the
+    # head's cache fits 16 chunks); grid: the cooperative launch with a grid
+    # barrier; split: separate score / weight / combine launches
+    if request.param != "cluster":
+        monkeypatch.setenv("LSSAR_DECODE_PATH", request.param)
+    else:
+        monkeypatch.delenv("LSSAR_DECODE_PATH", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("d", [64, 128])
-def test_decode_many_heads(torch_mod, d):
-    # 768 heads: more CTAs than can be resident at once, so the step runs as
-    # separate score / weight / combine launches instead of one cooperative
-    # launch; sampled heads against the oracle
+def test_decode_many_heads(torch_mod, d, decode_path):
+    # 768 heads (more CTAs than can be resident at once on the grid path, which
+    # then runs as three launches); sampled heads against the oracle
     B, H, L = 8, 96, 300
     qb, kb, vb = make_qkv(B, H, L, d, seed=d)
     for mode, p in [(MODE_LSSAR, 15), (MODE_SOFTMAX, 1)]:
@@ -91,9 +102,10 @@ def test_decode_many_heads(torch_mod, d):
             assert np.abs(got[b, h] - ref).max() <= tol(mode, p), (d, mode, b, h)
 
 
-def test_decode_long_single_head(torch_mod):
-    # one head, 40000 keys: hundreds of chunks of one head meet at the grid
-    # barrier and the last one to finish combines them
+def test_decode_long_single_head(torch_mod, decode_path):
+    # one head, 40000 keys: a cluster of 16 chunks, or (grid path) hundreds of
+    # chunks of one head that meet at the grid barrier, the last one to finish
+    # combining them
     B, H, L, d = 1, 1, 40000, 64
     qb, kb, vb = make_qkv(B, H, L, d, seed=5)
     qf, kf, vf = (bf16_bits_to_f64(t[0, 0]) for t in (qb, kb, vb))
@@ -101,3 +113,14 @@ def test_decode_long_single_head(torch_mod):
         got = decode(torch_mod, qb, kb, vb, p, mode)
         ref = attention_forward(qf, kf, vf, mode, p, rows=np.array([L]))[0]
         assert np.abs(got[0, 0] - ref).max() <= tol(mode, p), mode
+
+
+def test_decode_beyond_cluster_reach(torch_mod):
+    # 70000 keys in one head: more than 16 chunks of 4096, so the default path
+    # is the cooperative launch
+    B, H, L, d = 1, 1, 70000, 64
+    qb, kb, vb = make_qkv(B, H, L, d, seed=11)
+    qf, kf, vf = (bf16_bits_to_f64(t[0, 0]) for t in (qb, kb, vb))
+    got = decode(torch_mod, qb, kb, vb, 15, MODE_LSSAR)
+    ref = attention_forward(qf, kf, vf, MODE_LSSAR, 15, rows=np.array([L]))[0]
+    assert np.abs(got[0, 0] - ref).max() <= 5e-2
