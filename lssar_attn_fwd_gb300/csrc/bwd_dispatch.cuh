@@ -27,7 +27,7 @@ cudaError_t launch_kernel(const Maps &m, const Params &prm, int grid, cudaStream
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, stream>>>(m.x1, m.x2, m.y1, m.y2, prm);
+    kern<<<grid, Tmem<D, PASS>::kThreads, smem, stream>>>(m.x1, m.x2, m.y1, m.y2, prm);
     return cudaGetLastError();
 }
 

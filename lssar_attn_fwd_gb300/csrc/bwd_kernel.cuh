@@ -61,11 +61,10 @@ using OffDiag = std::false_type;   // a tile without masked elements
 
 constexpr int kBM = 128;                  // anchor rows of an item (TMEM lanes)
 constexpr int kBN = 128;                  // partner rows of a streamed tile
-constexpr int kThreads = 576;
 constexpr int kMathWarp0 = 2;
 constexpr int kMathThreads = 4 * kBM;
+constexpr int kAccWarp = 18;      // accumulation issuer, when there are two issuers
 constexpr int kItemQ = 4;
-constexpr uint32_t kItemConsumers = 1 + kMathThreads;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kSuspendNs = 1000000;
 
@@ -111,6 +110,12 @@ struct Tmem {
     static constexpr uint32_t kS = 0, kDP = 128, kAcc1 = 256, kAcc2 = 256 + D;
     static constexpr uint32_t kA1 = kAlias ? 0u : (PASS == kRowPass ? 256u + D : 256u + 2 * D);
     static constexpr uint32_t kA2 = kAlias ? 128u : kA1 + 64;
+    // Two MMA issuers (warp 1: S and dP; warp kAccWarp: the accumulations)
+    // unless A is written over S / dP, where the next scores must follow the
+    // accumulation in one issue order.
+    static constexpr int kIssuers = kAlias ? 1 : 2;
+    static constexpr int kThreads = 576 + 32 * (kIssuers - 1);
+    static constexpr uint32_t kItemConsumers = kIssuers + kMathThreads;
 };
 static_assert(Tmem<128, kRowPass>::kA1 + 64 <= 512 && Tmem<64, kColPass>::kA2 + 64 <= 512, "TMEM");
 
@@ -241,7 +246,7 @@ __device__ __forceinline__ uint32_t pack_ds(float lo, float hi) {
 }
 
 template <int D, int MODE, int PK, int PASS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Tmem<D, PASS>::kThreads, 1)
 lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant__ CUtensorMap tmX2,
                  const __grid_constant__ CUtensorMap tmY1, const __grid_constant__ CUtensorMap tmY2,
                  const Params prm) {
@@ -271,7 +276,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
         ptx::mbar_init(ptx::smem_u32(&bars->x_empty), 1);
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(ptx::smem_u32(&bars->ring_full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->ring_empty[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->ring_empty[s]), T::kIssuers);   // one commit per issuer
         }
         ptx::mbar_init(ptx::smem_u32(&bars->s_full), 1);
         ptx::mbar_init(ptx::smem_u32(&bars->s_free), kMathThreads);
@@ -282,7 +287,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
         ptx::mbar_init(ptx::smem_u32(&bars->red), kMathThreads);
         for (int s = 0; s < kItemQ; ++s) {
             ptx::mbar_init(ptx::smem_u32(&bars->item_full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->item_empty[s]), kItemConsumers);
+            ptx::mbar_init(ptx::smem_u32(&bars->item_empty[s]), T::kItemConsumers);
         }
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
@@ -407,10 +412,15 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 wait_bar(ptx::smem_u32(&bars->x_full), (x_cnt - 1) & 1, bars, prm.err, kErrDrain, false);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // (the whole warp runs the loop; one elected lane issues the MMAs and
-        // commits)
+    } else if (warp == 1 || (T::kIssuers == 2 && warp == kAccWarp)) {
+        // ------------------------------------------------------------ MMA issuers
+        // With two issuers, warp 1 issues S and dP of every partner tile and
+        // warp kAccWarp the accumulations, so the two chains of waits and issues
+        // overlap; both walk the whole stage sequence and commit every stage's
+        // release (a stage is free after one commit per issuer).  With one
+        // issuer, warp 1 issues everything in one order.  The whole warp runs
+        // the loop; one elected lane issues the MMAs and commits.
+        const bool do_scores = warp == 1;
         {
             uint32_t ring_idx = 0, x_cnt = 0, qi = 0;
             uint32_t sf_phase = 0, af_phase = 0, accf_phase = 0;
@@ -489,10 +499,51 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 int bh, at, p0, p1;
                 decode(item, bh, at, p0, p1);
                 const int n = p1 - p0;
+                uint32_t slot;
+                if constexpr (T::kIssuers == 2) {
+                    if (do_scores) {
+                        if (!(ok = wait_all(ptx::smem_u32(&bars->x_full), x_cnt & 1, kErrXFull))) break;
+                        ++x_cnt;
+                        ptx::tc_fence_after();
+                        // row pass: the statistics sweep, then the accumulation sweep
+                        for (int sweep = 0; ok && sweep < kPasses; ++sweep)
+                            for (int t = 0; t < n; ++t) {
+                                if (!(ok = acquire(slot)) || !(ok = touch_s())) break;
+                                issue_scores(slot);
+                                commit(&bars->ring_empty[slot]);
+                            }
+                        if (!ok) break;
+                        commit(&bars->x_empty);
+                    } else {
+                        if (kRow)   // the statistics sweep's stages: released as they arrive
+                            for (int t = 0; ok && t < n; ++t) {
+                                if (!(ok = acquire(slot))) break;
+                                commit(&bars->ring_empty[slot]);
+                            }
+                        for (int t = 0; ok && t < n; ++t) {
+                            if (!(ok = acquire(slot))) break;
+                            if (!(ok = wait_all(ptx::smem_u32(&bars->a_full), af_phase, kErrAFull))) break;
+                            af_phase ^= 1;
+                            ptx::tc_fence_after();
+                            if (t == 0 && acc_pending) {
+                                if (!(ok = wait_all(ptx::smem_u32(&bars->acc_free), accf_phase, kErrAccFree))) break;
+                                accf_phase ^= 1;
+                                acc_pending = false;
+                                ptx::tc_fence_after();
+                            }
+                            issue_acc(slot, t > 0);
+                            commit(&bars->a_free);
+                            commit(&bars->ring_empty[slot]);
+                        }
+                        if (!ok) break;
+                        commit(&bars->acc_full);
+                        acc_pending = true;
+                    }
+                    continue;
+                }
                 if (!(ok = wait_all(ptx::smem_u32(&bars->x_full), x_cnt & 1, kErrXFull))) break;
                 ++x_cnt;
                 ptx::tc_fence_after();
-                uint32_t slot;
                 if (kRow) {
                     // pass 1: scores only
                     for (int t = 0; ok && t < n; ++t) {
