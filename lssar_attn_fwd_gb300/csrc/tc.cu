@@ -37,6 +37,9 @@ __global__ void __launch_bounds__(256) normalize_rows_fp16(const __nv_bfloat16 *
                                                            long long rows, unsigned *counter, int L,
                                                            float qmul) {
     constexpr int G = D / 8;
+    // the attention kernel may launch now; it waits for this grid's completion
+    // before it reads anything written here
+    ptx::launch_dependents();
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (tid == 0) *counter = 0u;
     const long long r = tid / G;

@@ -22,8 +22,19 @@ cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CU
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (e != cudaSuccess) return e;
-    kern<<<grid, Cfg<D>::kThreads, smem, stream>>>(mq, mk, mv, prm);
-    return cudaGetLastError();
+    // a programmatic dependent of the prologue: the launch and the kernel's
+    // setup overlap the prologue's tail (the kernel waits before reading)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Cfg<D>::kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, prm);
 }
 
 // Re-weighting modes: compile-time power chains for p in {1, 2, 3, 15},

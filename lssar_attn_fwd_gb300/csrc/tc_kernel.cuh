@@ -451,6 +451,10 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // The launch may overlap the normalisation prologue (a programmatic
+    // dependent launch): everything above is local setup; the prologue's
+    // outputs (q-hat, k-hat, the zeroed work counter) are read only after this.
+    ptx::grid_dependency_wait();
 
     const int BH = prm.BH;
     auto decode = [&](int item, int &bh, int &m) {

@@ -110,6 +110,18 @@ __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- dependent launches
+
+// In a kernel launched as a programmatic dependent of the previous kernel in
+// its stream: wait until that kernel has completed and its memory writes are
+// visible (a no-op in a kernel launched without the attribute).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream, if launched as a programmatic
+// dependent, start its launch now (it still waits for this kernel's
+// completion before reading what this kernel writes).
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------- clusters
 
 // Barrier of all threads of all CTAs of the cluster, with release / acquire
