@@ -50,7 +50,7 @@
 //               pairs) to TMEM, and stores its half of the output row.  Each SM
 //               sub-partition therefore runs four math warps.  The two halves of
 //               a row combine their partial sums and maxima once per item
-//               through shared memory.
+//               through shared memory (a per-tile mbarrier, bounded wait).
 // The control warps run their loops warp-wide (one elected lane issues each
 // copy, MMA and commit).  Eighteen or nineteen warps put five on some SM
 // sub-partitions, which caps the registers at 96 per thread.
@@ -93,7 +93,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a stuck wait gives up after
 
 // Error codes written to the device error word (first failure wins).
 enum : unsigned { kErrQFull = 1, kErrQEmpty, kErrKvFull, kErrKvEmpty, kErrSFull, kErrSFree,
-                  kErrOFull, kErrOFree, kErrItem, kErrPFull, kErrPFree, kErrDrain };
+                  kErrOFull, kErrOFree, kErrItem, kErrPFull, kErrPFree, kErrDrain, kErrHalves };
 
 // Shared-memory descriptor strides.  K-major tiles (Q, K): rows of 128 bytes,
 // 8-row groups 1024 bytes apart.  MN-major V tiles: 16 keys per MMA = 2048
@@ -154,6 +154,7 @@ constexpr uint32_t kTileThreads = 2 * kBM;           // the two warpgroups of on
 struct __align__(8) Barriers {
     uint64_t q_full[2], q_empty[2];
     uint64_t s_full[2], s_free[2], o_full[2], o_free[2], p_full[2], p_free[2];
+    uint64_t halves[2];   // per Q tile: both column halves have written their row partials
     uint64_t kv_full[8], kv_empty[8];
     uint64_t item_full[kItemQ], item_empty[kItemQ];
     int item_q[kItemQ];
@@ -166,10 +167,6 @@ struct __align__(8) Barriers {
 };
 
 static_assert(sizeof(Barriers) <= 8192, "barrier block too large");
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 
 constexpr uint32_t kSuspendNs = 1000000;   // hardware suspend per try_wait (upper bound)
 
@@ -430,6 +427,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::mbar_init(ptx::smem_u32(&bars->o_free[w]), kTileThreads);
             ptx::mbar_init(ptx::smem_u32(&bars->p_full[w]), kTileThreads);
             ptx::mbar_init(ptx::smem_u32(&bars->p_free[w]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->halves[w]), kTileThreads);
         }
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
@@ -748,7 +746,8 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t s_free = ptx::smem_u32(&bars->s_free[w]);
         const uint32_t o_full = ptx::smem_u32(&bars->o_full[w]);
         const uint32_t o_free = ptx::smem_u32(&bars->o_free[w]);
-        const int pair_bar = 1 + w;                 // named barrier of this tile's two halves
+        const uint32_t halves = ptx::smem_u32(&bars->halves[w]);   // this tile's two column halves
+        uint32_t hv_phase = 0;
         uint32_t sf_phase = 0, of_phase = 0, qi = 0;
         const float log2e = 1.4426950408889634f;
         auto wait_warp = [&](uint32_t bar, uint32_t parity, unsigned code) -> bool {
@@ -832,7 +831,10 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if constexpr (MODE == kLssar)
                         bars->x_s1[w][h][t] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + s1_log;
                 }
-                named_bar_sync(pair_bar, kTileThreads);
+                // both halves' partials are in shared memory (bounded wait)
+                ptx::mbar_arrive(halves);
+                if (!(ok = wait_warp(halves, hv_phase, kErrHalves))) break;
+                hv_phase ^= 1;
                 const float m0 = bars->x_m[w][0][t], m1 = bars->x_m[w][1][t];
                 const float mxr = fmaxf(m0, m1);
                 if constexpr (MODE == kSoftmax) {
@@ -946,7 +948,9 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             if (!ok) break;
             bars->x_s2[w][h][t] = (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
-            named_bar_sync(pair_bar, kTileThreads);
+            ptx::mbar_arrive(halves);
+            if (!(ok = wait_warp(halves, hv_phase, kErrHalves))) break;
+            hv_phase ^= 1;
             const float s2 = bars->x_s2[w][0][t] + bars->x_s2[w][1][t];
             // epilogue: this half's D/2 output columns
             if (!(ok = wait_warp(o_full, of_phase, kErrOFull))) break;
