@@ -778,9 +778,10 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 // ---------------- column pass: key row arow, query tiles at..n_tiles-1
                 const float R = __uint_as_float(prm.rmax[bh]);
                 const float invR = R > 0.f ? 1.f / R : 0.f;
-                // rec: this tile's query records, field-major ([field][128 queries]).
+                // rec: shared address of this tile's query records, field-major
+                // ([field][128 queries]).
                 // A warpgroup's 32 columns go in two 16-column halves.
-                auto col_half = [&](const uint32_t (&rs)[16], const uint32_t (&rd)[16], const float *rec,
+                auto col_half = [&](const uint32_t (&rs)[16], const uint32_t (&rd)[16], uint32_t rec,
                                     int col0, uint32_t (&w1)[8], uint32_t (&w2)[8], auto diag) {
 #pragma unroll
                     for (int c = 0; c < 16; c += 4) {
@@ -789,7 +790,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
                             if (k > 1 || kRaw)   // a and m: softmax normalisers only
-                                f[k] = *reinterpret_cast<const float4 *>(rec + k * kBN + q0);
+                                f[k] = ptx::ld_shared_v4(rec + 4u * (k * kBN + q0));
                         // fields: 0 a, 1 m, 2 kappa, 3 beta, 4 1/W, 5 s F, 6 D, 7 s dS1, with
                         // s = a for the softmax normalisers and 1 for the normalised modes
                         // (their query operand carries a_i)
@@ -828,7 +829,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                     const uint32_t slot = ring_idx % NS, use = ring_idx / NS;
                     ++ring_idx;
                     if (!(ok = wait_warp(ptx::smem_u32(&bars->ring_full[slot]), use & 1, kErrRingFull))) break;
-                    const float *rec = reinterpret_cast<const float *>(ring + slot * C::kStageBytes + 2 * TB);
+                    const uint32_t rec = ptx::opaque_u32(ptx::smem_u32(ring + slot * C::kStageBytes + 2 * TB));
                     if constexpr (T::kAlias) {
                         // d = 128 (A over S / dP, released by the accumulation):
                         // one 16-column half in registers at a time

@@ -145,6 +145,28 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
     return v;
 }
 
+// 16-byte load from this CTA's shared memory by its 32-bit shared address
+// (a pointer rebuilt from an integer loses its address space, and the compiler
+// would issue a generic load, tracked like a global one).  Not volatile, so
+// that the compiler schedules it freely: the caller takes the address from
+// opaque_u32() after the barrier wait that makes the data visible, so that the
+// load cannot move above that wait.
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
+    float4 v;
+    asm("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "r"(addr));
+    return v;
+}
+
+// The value x, produced by a volatile instruction: code that depends on the
+// result stays after every earlier volatile asm (barrier waits).
+__device__ __forceinline__ uint32_t opaque_u32(uint32_t x) {
+    uint32_t y;
+    asm volatile("mov.b32 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // True in exactly one lane of the (converged) warp.  The single-thread
 // issue instructions (tcgen05.mma, tcgen05.commit, TMA copies) go under it
 // while the whole warp runs the surrounding control flow, so that addresses,
