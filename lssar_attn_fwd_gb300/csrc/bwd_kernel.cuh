@@ -257,7 +257,10 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
     constexpr bool kRaw = !uses_normalised_qk(MODE);
     constexpr bool kRow = PASS == kRowPass;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base as an offset from the array itself: a pointer
+    // rebuilt from an integer would lose the shared address space, and every
+    // access through it would compile to a generic load or store
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sX = smem;
     uint8_t *ring = smem + C::kRingOff;
     Barriers *bars = reinterpret_cast<Barriers *>(smem + C::kBarOff);
