@@ -434,8 +434,12 @@ def run_decode(args, mode, p):
     s = torch.cuda.current_stream()
     for _ in range(args.warmup):
         api.lssar_attn_decode(q, k, v, p=p, mode=mode, out=out)
+    plan = api.decode_plan(B, H, L, d)   # path, launches per step, chunking
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
     torch.cuda.synchronize()
+    t0 = time.time()
     for a, b in ev:
         if flush_each:
             flush.zero_()
@@ -443,6 +447,8 @@ def run_decode(args, mode, p):
         api.lssar_attn_decode(q, k, v, p=p, mode=mode, out=out)
         b.record(s)
     torch.cuda.synchronize()
+    t1 = time.time()
+    sampler.stop()
     ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
     gbs = cache_bytes / (ms * 1e-3) / 1e9
     try:
@@ -458,7 +464,9 @@ def run_decode(args, mode, p):
                           f"not flushed: the {cache_bytes / 2**20:.0f} MiB cache is over twice the L2 size")},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": f"{kind} hbm_gbs"},
-        "gpu_launches": 3 * args.steps}), flush=True)
+        "plan": plan,
+        "clocks": sampler.summary(t0, t1),
+        "gpu_launches": plan["launches"] * args.steps}), flush=True)
 
 
 def run_backward(args, wl, mode, p):

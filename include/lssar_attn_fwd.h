@@ -244,6 +244,19 @@ int lssar_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *ou
 int lssar_schedule_plan(int BH, int n_qtiles, int grid, int *first, int *tail_base);
 
 /*
+ * The launch plan of lssar_attn_decode for these sizes on the current device
+ * (host only: queries the device's SM count and occupancy, launches nothing).
+ * Outputs, each may be NULL: *path = 0 (one launch, a thread-block cluster per
+ * head), 1 (one cooperative launch) or 2 (three launches); *launches = the
+ * kernel launches one decode call makes (1, 1 or 3); *chunks = pieces of
+ * each head's cache; *chunk_rows = keys per piece (the last one shorter).
+ * The environment variable LSSAR_DECODE_PATH is honoured as by the call.
+ * Returns LSSAR_OK, LSSAR_ERR_SHAPE / LSSAR_ERR_HEADDIM on sizes the call
+ * rejects, or LSSAR_ERR_CUDA (no device).
+ */
+int lssar_decode_plan(int B, int H, int L, int d, int *path, int *launches, int *chunks, int *chunk_rows);
+
+/*
  * TEST ONLY: the failure path of the bounded waits.  Runs one decode step
  * (B=1 H=4 L=512 d=64, zero inputs, internal scratch) whose producer warps
  * withhold every copy, so that each wait of that launch gives up after its

@@ -26,6 +26,7 @@ _EXPORTS = (
     "lssar_attn_bwd_simt",
     "lssar_selftest_stall",
     "lssar_schedule_plan",
+    "lssar_decode_plan",
     "lssar_status_string",
     "lssar_device_error_word",
     "lssar_abi_version",
@@ -71,6 +72,8 @@ def load_library():
     lib.lssar_attn_fwd_profiled.restype = ctypes.c_int
     lib.lssar_schedule_plan.argtypes = [ctypes.c_int] * 3 + [ctypes.POINTER(ctypes.c_int)] * 2
     lib.lssar_schedule_plan.restype = ctypes.c_int
+    lib.lssar_decode_plan.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_int)] * 4
+    lib.lssar_decode_plan.restype = ctypes.c_int
     lib.lssar_selftest_stall.argtypes = [ctypes.c_void_p]
     lib.lssar_selftest_stall.restype = ctypes.c_int
     lib.lssar_status_string.argtypes = [ctypes.c_int]
@@ -277,6 +280,15 @@ def lssar_attn_fwd_profiled(q, k, v, p, mode, out, stream, ev_start, ev_main, ev
         ctypes.c_void_p(ev_end.cuda_event))
     _check(status)
     return out
+
+
+def decode_plan(B, H, L, d):
+    """Launch plan of lssar_attn_decode for these sizes on the current device:
+    dict(path=0 cluster | 1 cooperative | 2 three launches, launches,
+    chunks, chunk_rows)."""
+    vals = [ctypes.c_int(0) for _ in range(4)]
+    _check(load_library().lssar_decode_plan(B, H, L, d, *(ctypes.byref(v) for v in vals)))
+    return dict(zip(("path", "launches", "chunks", "chunk_rows"), (v.value for v in vals)))
 
 
 def selftest_stall():

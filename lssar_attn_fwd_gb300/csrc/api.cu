@@ -237,6 +237,19 @@ int lssar_attn_decode(const void *q, const void *k_cache, const void *v_cache, v
     return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
 }
 
+int lssar_decode_plan(int B, int H, int L, int d, int *path, int *launches, int *chunks, int *chunk_rows) {
+    if (B < 1 || H < 1 || L < 1 || L > (1 << 24)) return LSSAR_ERR_SHAPE;
+    if (d != 64 && d != 128) return LSSAR_ERR_HEADDIM;
+    if ((unsigned long long)B * H * L * d > (1ULL << 40)) return LSSAR_ERR_SHAPE;
+    lssar::DecodeRoute r;
+    if (lssar::decode_route(B * H, L, d, &r) != cudaSuccess) return LSSAR_ERR_CUDA;
+    if (path) *path = r.path;
+    if (launches) *launches = r.path == lssar::kDecodeSplit ? 3 : 1;
+    if (chunks) *chunks = r.chunks;
+    if (chunk_rows) *chunk_rows = r.chunk_rows;
+    return LSSAR_OK;
+}
+
 int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out, int B, int H,
                         int L, int d, int p, int mode, cudaStream_t stream) {
     lssar::Problem pr;

@@ -678,7 +678,10 @@ constexpr int kDecMaxCluster = 16;   // CTAs per cluster (above 8: non-portable 
 
 // Chunks per head for the cluster path: about one wave of kDecCtasPerSm CTAs
 // per SM when the heads allow it, at most kDecMaxCluster; 0 when a chunk would
-// exceed kDecMaxChunk rows (the path is then not available).
+// exceed kDecMaxChunk rows (the path is then not available).  (A rule that
+// counted whole waves of CTAs, each as long as its chunk plus a fixed cost,
+// split 768 heads of 2048 keys into three chunks and lost 7 %: the CTAs of
+// a partial wave share the memory bandwidth rather than leave it idle.)
 int cluster_chunks(int BH, int L, int sms, int *chunk_out) {
     long long nch = (long long)kDecCtasPerSm * sms / BH;
     if (nch < 1) nch = 1;
@@ -690,24 +693,30 @@ int cluster_chunks(int BH, int L, int sms, int *chunk_out) {
     return (int)((L + chunk - 1) / chunk);
 }
 
-// Launch of dec_cluster with nch CTAs per cluster, or cudaErrorNotSupported
-// when this device cannot place a cluster of that size (checked once per size).
-template <int D>
-cudaError_t launch_cluster(const DecodeProblem &pr, int BH, int chunk, int nch, unsigned *err, int withhold,
-                           cudaStream_t stream) {
-    const int smem = (int)sizeof(DecSmem);
+// Launch configuration of dec_cluster: BH clusters of nch CTAs (attr is the
+// caller's storage for the cluster-dimension attribute).
+cudaLaunchConfig_t cluster_config(int BH, int nch, cudaStream_t stream, cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nch, BH);
     cfg.blockDim = dim3(kDecBlock);
-    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.dynamicSmemBytes = sizeof(DecSmem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)nch;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Whether this device can place a cluster of nch dec_cluster CTAs (checked
+// once per size and device).
+template <int D>
+cudaError_t cluster_fits(int nch, bool *fits_out) {
+    const int smem = (int)sizeof(DecSmem);
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = cluster_config(1, nch, nullptr, attr);
     static PerDeviceOnce once[kDecMaxCluster + 1];
     int fits = 0;
     cudaError_t e = per_device_once(once[nch], &fits, [&](int &v) {
@@ -724,8 +733,16 @@ cudaError_t launch_cluster(const DecodeProblem &pr, int BH, int chunk, int nch, 
         v = clusters > 0 ? 1 : 0;
         return cudaSuccess;
     });
-    if (e != cudaSuccess) return e;
-    if (!fits) return cudaErrorNotSupported;
+    *fits_out = fits != 0;
+    return e;
+}
+
+// Launch of dec_cluster with nch CTAs per cluster (a size cluster_fits accepted).
+template <int D>
+cudaError_t launch_cluster(const DecodeProblem &pr, int BH, int chunk, int nch, unsigned *err, int withhold,
+                           cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = cluster_config(BH, nch, stream, attr);
     const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
     const auto *k = static_cast<const __nv_bfloat16 *>(pr.k);
     const auto *v = static_cast<const __nv_bfloat16 *>(pr.v);
@@ -735,21 +752,27 @@ cudaError_t launch_cluster(const DecodeProblem &pr, int BH, int chunk, int nch, 
 
 // One cooperative launch of dec_fused when every CTA of the grid can be
 // resident at once; otherwise the three-kernel sequence.
+// CTAs of dec_fused resident per SM (checked once per device; also sets the
+// shared-memory attributes of the grid-path kernels).
 template <int D>
-cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, int sms, float *z, float2 *part,
-                     float *opart, unsigned *sync, unsigned *err, int withhold, bool split, cudaStream_t stream) {
+cudaError_t grid_per_sm(int *per_sm) {
     const int smem = (int)sizeof(DecSmem);
     static PerDeviceOnce once;
-    int per_sm = 0;
-    cudaError_t e = per_device_once(once, &per_sm, [&](int &v) {
+    return per_device_once(once, per_sm, [&](int &v) {
         cudaError_t r = cudaFuncSetAttribute(dec_fused<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (r == cudaSuccess) r = cudaFuncSetAttribute(dec_scores<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (r == cudaSuccess) r = cudaFuncSetAttribute(dec_weights<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         return r != cudaSuccess ? r : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, dec_fused<D>, kDecBlock, smem);
     });
-    if (e != cudaSuccess) return e;
-    if (withhold && (split || (long long)nch * BH > (long long)per_sm * sms)) return cudaErrorInvalidConfiguration;
-    if (!split && (long long)nch * BH <= (long long)per_sm * sms) {
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeProblem &pr, int BH, int chunk, int nch, bool cooperative, float *z, float2 *part,
+                     float *opart, unsigned *sync, unsigned *err, int withhold, cudaStream_t stream) {
+    const int smem = (int)sizeof(DecSmem);
+    cudaError_t e;
+    if (withhold && !cooperative) return cudaErrorInvalidConfiguration;
+    if (cooperative) {
         e = cudaMemsetAsync(sync, 0, (size_t)(1 + BH) * sizeof(unsigned), stream);
         if (e != cudaSuccess) return e;
         const auto *q = static_cast<const __nv_bfloat16 *>(pr.q);
@@ -794,14 +817,10 @@ size_t decode_workspace_bytes(int BH, int L, int d, int sms) {
     return dec_layout(BH, L, d, (L + chunk - 1) / chunk).total;
 }
 
-cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream, bool withhold_copies) {
+cudaError_t decode_route(int BH, int L, int d, DecodeRoute *route) {
     int sms = 0;
     cudaError_t e = device_sms(&sms);
     if (e != cudaSuccess) return e;
-    unsigned *err = nullptr;
-    if ((e = error_word_ptr(&err)) != cudaSuccess) return e;
-    const int BH = pr.B * pr.H;
-    const int w = withhold_copies ? 1 : 0;
     // LSSAR_DECODE_PATH=grid | split steers the step away from the cluster
     // path (grid: the cooperative launch where possible; split: the three
     // launches), so that tests reach every path at small sizes.
@@ -809,22 +828,47 @@ cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream
     const bool no_cluster = force && (strcmp(force, "grid") == 0 || strcmp(force, "split") == 0);
     const bool split = force && strcmp(force, "split") == 0;
     int cchunk = 0;
-    const int cnch = no_cluster ? 0 : cluster_chunks(BH, pr.L, sms, &cchunk);
+    const int cnch = no_cluster ? 0 : cluster_chunks(BH, L, sms, &cchunk);
     if (cnch > 0) {
-        e = pr.d == 64 ? launch_cluster<64>(pr, BH, cchunk, cnch, err, w, stream)
-                       : launch_cluster<128>(pr, BH, cchunk, cnch, err, w, stream);
-        if (e != cudaErrorNotSupported) return e;
+        bool fits = false;
+        e = d == 64 ? cluster_fits<64>(cnch, &fits) : cluster_fits<128>(cnch, &fits);
+        if (e != cudaSuccess) return e;
+        if (fits) {
+            *route = DecodeRoute{kDecodeCluster, cnch, cchunk};
+            return cudaSuccess;
+        }
     }
-    const int chunk = choose_chunk(BH, pr.L, sms);
-    const int nch = (pr.L + chunk - 1) / chunk;
+    const int chunk = choose_chunk(BH, L, sms);
+    const int nch = (L + chunk - 1) / chunk;
+    int per_sm = 0;
+    e = d == 64 ? grid_per_sm<64>(&per_sm) : grid_per_sm<128>(&per_sm);
+    if (e != cudaSuccess) return e;
+    const bool coop = !split && (long long)nch * BH <= (long long)per_sm * sms;
+    *route = DecodeRoute{coop ? kDecodeGrid : kDecodeSplit, nch, chunk};
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream, bool withhold_copies) {
+    unsigned *err = nullptr;
+    cudaError_t e = error_word_ptr(&err);
+    if (e != cudaSuccess) return e;
+    const int BH = pr.B * pr.H;
+    const int w = withhold_copies ? 1 : 0;
+    DecodeRoute route;
+    if ((e = decode_route(BH, pr.L, pr.d, &route)) != cudaSuccess) return e;
+    if (route.path == kDecodeCluster)
+        return pr.d == 64 ? launch_cluster<64>(pr, BH, route.chunk_rows, route.chunks, err, w, stream)
+                          : launch_cluster<128>(pr, BH, route.chunk_rows, route.chunks, err, w, stream);
+    const int chunk = route.chunk_rows, nch = route.chunks;
+    const bool coop = route.path == kDecodeGrid;
     char *base = static_cast<char *>(ws);
     const DecLayout lay = dec_layout(BH, pr.L, pr.d, nch);
     float *z = reinterpret_cast<float *>(base);
     float2 *part = reinterpret_cast<float2 *>(base + lay.part);
     float *opart = reinterpret_cast<float *>(base + lay.opart);
     unsigned *sync = reinterpret_cast<unsigned *>(base + lay.sync);
-    return pr.d == 64 ? launch_d<64>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, w, split, stream)
-                      : launch_d<128>(pr, BH, chunk, nch, sms, z, part, opart, sync, err, w, split, stream);
+    return pr.d == 64 ? launch_d<64>(pr, BH, chunk, nch, coop, z, part, opart, sync, err, w, stream)
+                      : launch_d<128>(pr, BH, chunk, nch, coop, z, part, opart, sync, err, w, stream);
 }
 
 }  // namespace lssar

@@ -69,6 +69,15 @@ struct DecodeProblem {
     int B, H, L, d, p, mode;
 };
 size_t decode_workspace_bytes(int BH, int L, int d, int sms);
+// The path a decode step takes on the current device: one launch with a
+// thread-block cluster per head, one cooperative launch, or three launches;
+// each head's cache in `chunks` pieces of `chunk_rows` keys (the last one
+// shorter).
+enum { kDecodeCluster = 0, kDecodeGrid = 1, kDecodeSplit = 2 };
+struct DecodeRoute {
+    int path, chunks, chunk_rows;
+};
+cudaError_t decode_route(int BH, int L, int d, DecodeRoute *route);
 // withhold_copies: self-test of the failure path (the one-launch kernel issues
 // no copies, every wait of the launch runs into its bound).
 cudaError_t launch_decode(const DecodeProblem &pr, void *ws, cudaStream_t stream, bool withhold_copies = false);

@@ -124,6 +124,16 @@ def test_decode_invalid_arguments(lib):
     assert call_raw(f, Q, K, V, K + 64, 1, 2, 16, 64, 3, 2, 0) == -8   # out inside the key cache
 
 
+def test_decode_plan_invalid_arguments(lib):
+    import ctypes
+    out = [ctypes.c_int(0) for _ in range(4)]
+    refs = [ctypes.byref(v) for v in out]
+    assert lib.lssar_decode_plan(0, 2, 16, 64, *refs) == -2
+    assert lib.lssar_decode_plan(1, 2, 0, 64, *refs) == -2
+    assert lib.lssar_decode_plan(1, 2, (1 << 24) + 1, 64, *refs) == -2
+    assert lib.lssar_decode_plan(1, 2, 16, 96, *refs) == -3
+
+
 STATS, DQ, DK, DV, DOUT = 5 << 32, 6 << 32, 7 << 32, 8 << 32, 9 << 32
 
 

@@ -124,3 +124,35 @@ def test_decode_beyond_cluster_reach(torch_mod):
     got = decode(torch_mod, qb, kb, vb, 15, MODE_LSSAR)
     ref = attention_forward(qf, kf, vf, MODE_LSSAR, 15, rows=np.array([L]))[0]
     assert np.abs(got[0, 0] - ref).max() <= 5e-2
+
+
+def expected_cluster_split(BH, L, sms):
+    """The cluster path's split of each head's cache: about one wave of four
+    CTAs per SM (at least one chunk, at most 16), chunks a multiple of 64 keys
+    and at most 4096; None when no split fits."""
+    nch = min(max(4 * sms // BH, 1), 16)
+    chunk = -(-L // nch)
+    chunk = -(-chunk // 64) * 64
+    if chunk > 4096:
+        return None
+    return -(-L // chunk), chunk
+
+
+@pytest.mark.parametrize("B,H,L,d", [(8, 12, 16384, 64), (64, 12, 2048, 64), (1, 32, 32768, 128),
+                                     (4, 16, 4096, 128), (2, 3, 1, 64), (1, 1, 70000, 64)])
+def test_decode_plan(torch_mod, B, H, L, d, monkeypatch):
+    from lssar_attn_fwd_gb300 import api
+    monkeypatch.delenv("LSSAR_DECODE_PATH", raising=False)
+    sms = torch_mod.cuda.get_device_properties(0).multi_processor_count
+    plan = api.decode_plan(B, H, L, d)
+    exp = expected_cluster_split(B * H, L, sms)
+    if exp is None:   # longer than 16 chunks of 4096 keys: grid or three launches
+        assert plan["path"] in (1, 2) and plan["launches"] == (1 if plan["path"] == 1 else 3)
+    else:
+        assert (plan["path"], plan["launches"]) == (0, 1)
+        assert (plan["chunks"], plan["chunk_rows"]) == exp
+    assert plan["chunk_rows"] % 64 == 0 and plan["chunk_rows"] <= 4096
+    assert (plan["chunks"] - 1) * plan["chunk_rows"] < L <= plan["chunks"] * plan["chunk_rows"]
+    monkeypatch.setenv("LSSAR_DECODE_PATH", "split")
+    split = api.decode_plan(B, H, L, d)
+    assert (split["path"], split["launches"]) == (2, 3)
