@@ -234,19 +234,14 @@ int lssar_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *ou
 
 /*
  * Introspection of the attention kernel's work schedule (host only, no CUDA
- * call).  Work items are pairs of 128-row Q tiles of one head, numbered group
- * by group of `head_group` heads (the last group may have fewer, gs), longest
- * first within a group: item i is in group g = i / (head_group * n_pairs);
- * with j = i - g * head_group * n_pairs it is pair n_pairs - 1 - j / gs of
- * head g * head_group + j % gs.  The forward pass uses as head_group the
- * largest number of heads whose streamed K and V (4 * L * d bytes per head)
- * fit in 48 MB, at most BH, so that the tiles a head's pairs share stay in
- * L2.  CTA c of a grid of `grid` CTAs first processes first[2c] and then
- * first[2c+1] (-1: none), then the items from *tail_base on, as a global
- * counter hands them out.  first must hold 2*grid ints; 1 <= grid <= 256;
- * 1 <= head_group <= BH.  Returns LSSAR_OK, LSSAR_ERR_NULL or LSSAR_ERR_SHAPE.
+ * call).  Work items are pairs of 128-row Q tiles of one head, numbered
+ * longest first (item i: head i % BH, pair n_pairs - 1 - i / BH).  CTA c of a
+ * grid of `grid` CTAs first processes first[2c] and then first[2c+1] (-1:
+ * none), then the items from *tail_base on, as a global counter hands them
+ * out.  first must hold 2*grid ints; 1 <= grid <= 256.  Returns LSSAR_OK,
+ * LSSAR_ERR_NULL or LSSAR_ERR_SHAPE.
  */
-int lssar_schedule_plan(int BH, int n_qtiles, int grid, int head_group, int *first, int *tail_base);
+int lssar_schedule_plan(int BH, int n_qtiles, int grid, int *first, int *tail_base);
 
 /*
  * The launch plan of lssar_attn_decode for these sizes on the current device

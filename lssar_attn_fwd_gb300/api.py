@@ -70,7 +70,7 @@ def load_library():
         fn.restype = ctypes.c_int
     lib.lssar_attn_fwd_profiled.argtypes = fwd_args + [ctypes.c_void_p] * 3
     lib.lssar_attn_fwd_profiled.restype = ctypes.c_int
-    lib.lssar_schedule_plan.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_int)] * 2
+    lib.lssar_schedule_plan.argtypes = [ctypes.c_int] * 3 + [ctypes.POINTER(ctypes.c_int)] * 2
     lib.lssar_schedule_plan.restype = ctypes.c_int
     lib.lssar_decode_plan.argtypes = [ctypes.c_int] * 4 + [ctypes.POINTER(ctypes.c_int)] * 4
     lib.lssar_decode_plan.restype = ctypes.c_int

@@ -258,10 +258,9 @@ int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out, 
     return lssar::launch_simt(pr, stream) == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
 }
 
-int lssar_schedule_plan(int BH, int n_qtiles, int grid, int head_group, int *first, int *tail_base) {
+int lssar_schedule_plan(int BH, int n_qtiles, int grid, int *first, int *tail_base) {
     if (!first || !tail_base) return LSSAR_ERR_NULL;
-    return lssar::schedule_plan(BH, n_qtiles, grid, head_group, first, tail_base) == 0 ? LSSAR_OK
-                                                                                     : LSSAR_ERR_SHAPE;
+    return lssar::schedule_plan(BH, n_qtiles, grid, first, tail_base) == 0 ? LSSAR_OK : LSSAR_ERR_SHAPE;
 }
 
 int lssar_selftest_stall(cudaStream_t stream) {
@@ -310,6 +309,6 @@ int lssar_device_error_word(unsigned int *word) {
     return lssar::read_and_clear_error_word(word) == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
 }
 
-int lssar_abi_version(void) { return 10100; }
+int lssar_abi_version(void) { return 10000; }
 
 }  // extern "C"

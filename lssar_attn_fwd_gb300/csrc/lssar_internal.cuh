@@ -123,7 +123,7 @@ inline cudaError_t device_sms(int *sms) {
 // The attention kernel's work schedule for BH heads of n_qtiles Q tiles on
 // `grid` CTAs (host only): first[2c], first[2c+1] = the fixed items of CTA c
 // (-1: none), *tail_base = the first item handed out by the counter.
-int schedule_plan(int BH, int n_qtiles, int grid, int head_group, int *first, int *tail_base);
+int schedule_plan(int BH, int n_qtiles, int grid, int *first, int *tail_base);
 
 // Reads and clears the device error word of the current device.
 cudaError_t read_and_clear_error_word(unsigned int *word);

@@ -149,10 +149,8 @@ cudaError_t error_word_ptr(unsigned **out) {
 namespace {
 
 // Work schedule of the attention kernel for BH heads of n_qtiles Q tiles on
-// `grid` CTAs.  Items run group by group of G heads (head_group_for), longest
-// first within a group: with j = i - g G n_pairs in group g of gs heads, item
-// i is the Q-tile pair m = n_pairs-1 - j/gs of head g G + j%gs (G = BH: pair
-// n_pairs-1 - i/BH of head i%BH); its cost is modelled as the K tiles its two Q tiles
+// `grid` CTAs.  Item id i (longest first) is the Q-tile pair m = n_pairs-1 -
+// i/BH of head i%BH; its cost is modelled as the K tiles its two Q tiles
 // stream, (2m+1) + (2m+2) (one fewer tile when the second is past the end),
 // plus one tile of fixed cost.  Two schedules are simulated and the one with
 // the shorter makespan is used:
@@ -165,14 +163,11 @@ struct Schedule {
     std::vector<int> first;   // 2 per CTA, -1 for none
 };
 
-Schedule plan_schedule(int BH, int n_qtiles, int grid, int G) {
+Schedule plan_schedule(int BH, int n_qtiles, int grid) {
     const int n_pairs = (n_qtiles + 1) / 2;
     const long long N = (long long)BH * n_pairs;
     auto cost = [&](long long id) {
-        const long long per_group = (long long)G * n_pairs;
-        const long long g = id / per_group, j = id - g * per_group;
-        const long long gs = std::min<long long>(G, BH - g * G);
-        const int m = n_pairs - 1 - (int)(j / gs);
+        const int m = n_pairs - 1 - (int)(id / BH);
         const int qa = 2 * m, qb = 2 * m + 1;
         return (double)(qa + 1) + (qb < n_qtiles ? qb + 1 : 0) + 1.0;
     };
@@ -226,23 +221,14 @@ Schedule plan_schedule(int BH, int n_qtiles, int grid, int G) {
 
 // Schedules are computed once per (BH, n_qtiles, grid).
 std::mutex g_plan_mutex;
-std::map<std::tuple<int, int, int, int>, Schedule> g_plans;
+std::map<std::tuple<int, int, int>, Schedule> g_plans;
 
-const Schedule &schedule_for(int BH, int n_qtiles, int grid, int G) {
+const Schedule &schedule_for(int BH, int n_qtiles, int grid) {
     std::lock_guard<std::mutex> lock(g_plan_mutex);
-    const auto key = std::make_tuple(BH, n_qtiles, grid, G);
+    const auto key = std::make_tuple(BH, n_qtiles, grid);
     auto it = g_plans.find(key);
-    if (it == g_plans.end()) it = g_plans.emplace(key, plan_schedule(BH, n_qtiles, grid, G)).first;
+    if (it == g_plans.end()) it = g_plans.emplace(key, plan_schedule(BH, n_qtiles, grid)).first;
     return it->second;
-}
-
-// Heads whose streamed K and V (fp16 normalised keys, bf16 values) together
-// stay within 48 MB, so that the tiles re-read by a head's pairs hit in L2.
-int head_group_for(int BH, int L, int d) {
-    const long long per_head = (long long)L * d * 4;
-    long long g = (48LL << 20) / per_head;
-    if (g < 1) g = 1;
-    return (int)std::min<long long>(g, BH);
 }
 
 constexpr size_t kCounterBytes = 256;
@@ -293,7 +279,6 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
     prm.n_qtiles = (pr.L + tc::kBM - 1) / tc::kBM;
     prm.n_pairs = (prm.n_qtiles + 1) / 2;
     prm.n_items = BH * prm.n_pairs;
-    prm.head_group = head_group_for(BH, pr.L, pr.d);
     prm.ln_d = logf((float)pr.d);
     prm.p = pr.p;
     prm.H = pr.H;
@@ -308,7 +293,7 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
     if ((e = device_sms(&sms)) != cudaSuccess) return e;
     int grid = prm.n_items < sms ? prm.n_items : sms;
     if (grid > tc::kMaxCtas) grid = tc::kMaxCtas;
-    const Schedule &sch = schedule_for(BH, prm.n_qtiles, grid, prm.head_group);
+    const Schedule &sch = schedule_for(BH, prm.n_qtiles, grid);
     prm.tail_base = sch.tail_base;
     for (int c = 0; c < tc::kMaxCtas; ++c) {
         prm.first_items[c][0] = c < grid ? sch.first[2 * c] : -1;
@@ -322,9 +307,9 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
     return e;
 }
 
-int schedule_plan(int BH, int n_qtiles, int grid, int head_group, int *first, int *tail_base) {
-    if (BH < 1 || n_qtiles < 1 || grid < 1 || grid > tc::kMaxCtas || head_group < 1 || head_group > BH) return -1;
-    const Schedule &sch = schedule_for(BH, n_qtiles, grid, head_group);
+int schedule_plan(int BH, int n_qtiles, int grid, int *first, int *tail_base) {
+    if (BH < 1 || n_qtiles < 1 || grid < 1 || grid > tc::kMaxCtas) return -1;
+    const Schedule &sch = schedule_for(BH, n_qtiles, grid);
     for (int i = 0; i < 2 * grid; ++i) first[i] = sch.first[i];
     *tail_base = sch.tail_base;
     return 0;

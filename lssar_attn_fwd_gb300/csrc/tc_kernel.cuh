@@ -112,7 +112,6 @@ struct Params {
     int n_qtiles;    // ceil(L / 128)
     int n_pairs;     // ceil(n_qtiles / 2)
     int n_items;     // BH * n_pairs
-    int head_group;  // items run group by group of this many heads (longest first within a group)
     float ln_d;      // ln(d)
     int p;           // re-weighting exponent (used by the generic power path)
     int H;           // heads per batch entry (for the per-head exponents)
@@ -457,11 +456,8 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
     const int BH = prm.BH;
     auto decode = [&](int item, int &bh, int &m) {
-        const int per_group = prm.head_group * prm.n_pairs;
-        const int g = item / per_group, j = item - g * per_group;
-        const int gs = min(prm.head_group, BH - g * prm.head_group);
-        m = prm.n_pairs - 1 - j / gs;   // longest pairs first within the group
-        bh = g * prm.head_group + j % gs;
+        m = prm.n_pairs - 1 - item / BH;   // longest pairs first
+        bh = item % BH;
     };
     // Consumer side of the work-item queue: returns false on a timed-out wait.
     auto next_item = [&](uint32_t &qi, int &item, bool arrive = true) -> bool {

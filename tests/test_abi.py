@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.lssar_abi_version() >= 10100
+    assert lib.lssar_abi_version() >= 10000
 
 
 def call(lib, name="lssar_attn_fwd", q=Q, k=K, v=V, out=OUT, B=1, H=1, L=16, d=64, p=3, mode=2):
@@ -177,17 +177,15 @@ def test_backward_invalid_arguments(lib, name):
     assert c(6, DQ + 256) == -8                       # dk overlaps dq
 
 
-@pytest.mark.parametrize("BH,n_qtiles,grid,G", [(12, 64, 152, 12), (96, 8, 152, 96), (64, 32, 152, 64),
-                                                (64, 32, 152, 24), (12, 128, 152, 12), (8, 64, 152, 8),
-                                                (1, 1, 1, 1), (3, 5, 7, 2), (5, 63, 152, 5), (200, 2, 152, 200),
-                                                (200, 2, 152, 7)])
-def test_schedule_covers_every_item_once(lib, BH, n_qtiles, grid, G):
+@pytest.mark.parametrize("BH,n_qtiles,grid", [(12, 64, 152), (96, 8, 152), (64, 32, 152), (12, 128, 152),
+                                              (8, 64, 152), (1, 1, 1), (3, 5, 7), (5, 63, 152), (200, 2, 152)])
+def test_schedule_covers_every_item_once(lib, BH, n_qtiles, grid):
     n_pairs = (n_qtiles + 1) // 2
     n_items = BH * n_pairs
     grid = min(grid, n_items)
     first = (ctypes.c_int * (2 * grid))()
     tail = ctypes.c_int(0)
-    assert lib.lssar_schedule_plan(BH, n_qtiles, grid, G, first, ctypes.byref(tail)) == 0
+    assert lib.lssar_schedule_plan(BH, n_qtiles, grid, first, ctypes.byref(tail)) == 0
     fixed = [x for x in first if x >= 0]
     assert len(fixed) == len(set(fixed))
     # the fixed items are exactly [0, tail); the counter serves [tail, n_items)
@@ -203,7 +201,7 @@ def test_schedule_pairs_long_with_short_items(lib):
     BH, n_qtiles, grid = 12, 64, 152
     first = (ctypes.c_int * (2 * grid))()
     tail = ctypes.c_int(0)
-    assert lib.lssar_schedule_plan(BH, n_qtiles, grid, BH, first, ctypes.byref(tail)) == 0
+    assert lib.lssar_schedule_plan(BH, n_qtiles, grid, first, ctypes.byref(tail)) == 0
     cost = lambda i: 4 * (31 - i // BH) + 3   # noqa: E731  K tiles of the pair's two Q tiles
     loads = [sum(cost(x) for x in (first[2 * c], first[2 * c + 1]) if x >= 0) for c in range(grid)]
     mean = sum(cost(i) for i in range(BH * 32)) / grid
@@ -213,8 +211,6 @@ def test_schedule_pairs_long_with_short_items(lib):
 def test_schedule_rejects_bad_arguments(lib):
     first = (ctypes.c_int * 2)()
     tail = ctypes.c_int(0)
-    assert lib.lssar_schedule_plan(0, 4, 1, 1, first, ctypes.byref(tail)) == -2
-    assert lib.lssar_schedule_plan(1, 4, 300, 1, first, ctypes.byref(tail)) == -2
-    assert lib.lssar_schedule_plan(4, 4, 1, 0, first, ctypes.byref(tail)) == -2
-    assert lib.lssar_schedule_plan(4, 4, 1, 5, first, ctypes.byref(tail)) == -2
-    assert lib.lssar_schedule_plan(1, 4, 1, 1, None, ctypes.byref(tail)) == -1
+    assert lib.lssar_schedule_plan(0, 4, 1, first, ctypes.byref(tail)) == -2
+    assert lib.lssar_schedule_plan(1, 4, 300, first, ctypes.byref(tail)) == -2
+    assert lib.lssar_schedule_plan(1, 4, 1, None, ctypes.byref(tail)) == -1
