@@ -173,6 +173,30 @@ def test_needle_large_p_is_argmax(torch_mod):
     assert close[:, :, 64:].mean() > 0.95
 
 
+@pytest.mark.parametrize("p", [200, 1024])
+def test_largest_exponents(torch_mod, p):
+    # up to the largest exponent the C ABI accepts (generic power path): on
+    # the needle structure (one key clearly above the rest) the re-weighted
+    # rows are well conditioned, and every sampled row must match the oracle;
+    # the decode step must match the oracle's last row
+    from lssar_attn_fwd_gb300 import api
+    torch = torch_mod
+    B, H, L, d = 1, 2, 1024, 64
+    qb, kb, vb = make_qkv(B, H, L, d, seed=5, structure="needle")
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    got = run(torch, qb, kb, vb, p, MODE_LSSAR)
+    rows = np.unique(np.concatenate([np.arange(1, 9), sample_rows(L, seed=6)]))
+    q_last = to_dev(torch, np.ascontiguousarray(qb[:, :, -1]))
+    dec = api.lssar_attn_decode(q_last, to_dev(torch, kb), to_dev(torch, vb), p=p, mode=MODE_LSSAR)
+    torch.cuda.synchronize()
+    dec = dec.float().cpu().numpy().astype(np.float64)
+    for h in range(H):
+        ref = attention_forward(qf[0, h], kf[0, h], vf[0, h], MODE_LSSAR, p, rows=rows)
+        assert np.abs(got[0, h, rows - 1] - ref).max() <= tol(MODE_LSSAR, p), (p, h)
+        assert np.abs(dec[0, h] - ref[-1]).max() <= tol(MODE_LSSAR, p), (p, h)
+    check_error_word()
+
+
 def test_tc_matches_simt_full_size(torch_mod):
     # Consistency between the two GPU implementations on every row (an extra
     # check beside the oracle parity above).
