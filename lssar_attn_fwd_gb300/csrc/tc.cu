@@ -27,8 +27,12 @@ __device__ unsigned g_error_word;
 // With qmul != 0 query row i (1-based within its head) is also multiplied by
 // qmul * ln i, so that the score product yields z = qmul ln i qh.kh directly
 // (qmul = +-log2(e) ln d: the length scale in log2 units).  Each row is
-// handled by D/8 consecutive threads, 8 elements each.  Thread 0 also zeroes
-// the attention kernel's work counter.
+// handled by D/16 consecutive threads, 16 elements each: both 16-byte loads
+// of a thread are in flight together, so that enough bytes are in flight per
+// SM to keep this HBM-bound pass near the copy bandwidth.  Thread 0 also
+// zeroes the attention kernel's work counter.
+constexpr int kNormElems = 16;   // elements per thread
+
 template <int D>
 __global__ void __launch_bounds__(256) normalize_rows_fp16(const __nv_bfloat16 *__restrict__ q,
                                                            const __nv_bfloat16 *__restrict__ k,
@@ -36,7 +40,7 @@ __global__ void __launch_bounds__(256) normalize_rows_fp16(const __nv_bfloat16 *
                                                            __half *__restrict__ kh,
                                                            long long rows, unsigned *counter, int L,
                                                            float qmul) {
-    constexpr int G = D / 8;
+    constexpr int G = D / kNormElems;
     // the attention kernel may launch now; it waits for this grid's completion
     // before it reads anything written here
     ptx::launch_dependents();
@@ -47,39 +51,48 @@ __global__ void __launch_bounds__(256) normalize_rows_fp16(const __nv_bfloat16 *
     const bool live = r < 2 * rows;
     const bool is_k = r >= rows;
     const long long rr = is_k ? r - rows : r;
-    float x[8];
+    float x[kNormElems];
     float ss = 0.f;
     if (live) {
-        const __nv_bfloat16 *src = (is_k ? k : q) + rr * D + part * 8;
-        const uint4 u = *reinterpret_cast<const uint4 *>(src);
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+        const uint4 *src = reinterpret_cast<const uint4 *>((is_k ? k : q) + rr * D + part * kNormElems);
+        uint4 u[2];
+        u[0] = src[0];
+        u[1] = src[1];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(h[e]);
-            x[2 * e] = f.x;
-            x[2 * e + 1] = f.y;
+        for (int c = 0; c < 2; ++c) {
+            const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u[c]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(h[e]);
+                x[8 * c + 2 * e] = f.x;
+                x[8 * c + 2 * e + 1] = f.y;
+            }
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+        for (int e = 0; e < kNormElems; ++e) ss = fmaf(x[e], x[e], ss);
     }
 #pragma unroll
     for (int o = G / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (!live) return;
     float inv = 1.f / fmaxf(sqrtf(ss), 1e-12f);
     if (!is_k && qmul != 0.f) inv *= qmul * logf((float)(rr % L + 1));
-    uint4 u;
-    __half2 *h = reinterpret_cast<__half2 *>(&u);
+    uint4 *dst = reinterpret_cast<uint4 *>((is_k ? kh : qh) + rr * D + part * kNormElems);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(x[2 * e] * inv, x[2 * e + 1] * inv);
-    __half *dst = (is_k ? kh : qh) + rr * D + part * 8;
-    *reinterpret_cast<uint4 *>(dst) = u;
+    for (int c = 0; c < 2; ++c) {
+        uint4 u;
+        __half2 *h = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            h[e] = __floats2half2_rn(x[8 * c + 2 * e] * inv, x[8 * c + 2 * e + 1] * inv);
+        dst[c] = u;
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_normalize_fp16(const void *q, const void *k, void *qh, void *kh, long long rows,
                                   int d, unsigned *counter, cudaStream_t stream, int L, float qmul) {
-    const long long threads = 2 * rows * (d / 8);
+    const long long threads = 2 * rows * (d / kNormElems);
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const auto *qb = static_cast<const __nv_bfloat16 *>(q);
