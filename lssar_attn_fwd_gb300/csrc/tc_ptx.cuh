@@ -159,6 +159,25 @@ __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
     return v;
 }
 
+// 4-byte shared-memory accesses by 32-bit shared address, kept in program
+// order with the barrier operations around them (volatile, memory clobber).
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ int ld_shared_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_s32(uint32_t addr, int v) {
+    asm volatile("st.shared.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // The value x, produced by a volatile instruction: code that depends on the
 // result stays after every earlier volatile asm (barrier waits).
 __device__ __forceinline__ uint32_t opaque_u32(uint32_t x) {
