@@ -67,11 +67,12 @@ def peaks():
 
 
 def kernel_source_sha():
-    """Hash of the attention kernel's device sources (the kernel template and the
-    headers only it uses), to tell whether recorded counters still apply."""
+    """Hash of the attention kernel's device sources (the kernel template, the
+    headers it includes and its launch dispatch), to tell whether recorded
+    counters still apply."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("tc_kernel.cuh", "softplus_poly.cuh"):
+    for name in ("tc_kernel.cuh", "softplus_poly.cuh", "tc_ptx.cuh", "lssar_internal.cuh", "tc_dispatch.cuh"):
         with open(os.path.join(ROOT, "lssar_attn_fwd_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
