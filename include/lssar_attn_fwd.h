@@ -75,6 +75,13 @@ typedef enum {
  *             ignored in modes 0, 1).
  *   mode    : lssar_mode_t.
  * Returns LSSAR_OK or a negative lssar_status_t.
+ * Numerics of LSSAR mode with p >= 4: the weight pass evaluates the softplus
+ * of a row as z + 2^-|z| / ln 2 (one exponential, z = log2(e) x) instead of
+ * log2(1 + 2^z) when a bound computed from the row's statistics (its
+ * threshold, spread, length and p) guarantees that the row's weights change
+ * in sum by at most 2e-4 of their total (the output by at most 4e-4 max|v|);
+ * other rows keep log2(1 + 2^z).  Setting LSSAR_EXACT_WEIGHTS=1 in the
+ * environment keeps every row on log2(1 + 2^z) (read at each call).
  */
 int lssar_attn_fwd(const void *q, const void *k, const void *v, void *out,
                    int B, int H, int L, int d, int p, int mode, cudaStream_t stream);

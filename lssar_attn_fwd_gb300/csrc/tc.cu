@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <functional>
 #include <map>
 #include <mutex>
@@ -296,6 +297,10 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
     prm.p = pr.p;
     prm.H = pr.H;
     prm.per_head = pr.p_head ? 1 : 0;
+    // LSSAR_EXACT_WEIGHTS=1 keeps every row on the two-transcendental softplus
+    // in pass 2 (a cross-check of the one-exponential weights)
+    const char *exact = getenv("LSSAR_EXACT_WEIGHTS");
+    prm.exact_weights = (exact != nullptr && exact[0] == '1') ? 1 : 0;
     for (int h = 0; h < tc::kMaxHeadsP; ++h) prm.p_head[h] = (pr.p_head && h < pr.H) ? pr.p_head[h] : pr.p;
     prm.out = static_cast<__nv_bfloat16 *>(pr.out);
     prm.stats = reinterpret_cast<float4 *>(pr.stats);

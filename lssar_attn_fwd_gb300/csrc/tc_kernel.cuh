@@ -116,6 +116,7 @@ struct Params {
     int p;           // re-weighting exponent (used by the generic power path)
     int H;           // heads per batch entry (for the per-head exponents)
     int per_head;    // 1: head h uses p_head[h] (generic power path only)
+    int exact_weights;   // 1: LSSAR rows never take the one-exponential weights
     int p_head[kMaxHeadsP];
     // Work schedule: CTA c first processes first_items[c][0], then
     // first_items[c][1] (-1: none), then items tail_base, tail_base + 1, ...
@@ -286,8 +287,57 @@ struct RowConst {
     float kappa;   // LSSAR slope
     float beta;    // LSSAR offset
     float m;       // softmax: row maximum of z
+    float ck;      // LSSAR one-exponential weights: kappa / ln 2
     bool uniform;  // re-weighted row read as all-zero (prefix mean)
+    bool fast;     // LSSAR: the one-exponential weights meet the error bound on this row
 };
+
+// LSSAR weights with one exponential per element.  For z >= 0,
+// sp2(z) = z + log2(1 + u) with u = 2^-z, and log2(1 + u) <= u / ln 2 with a
+// gap of at most u^2 / (2 ln 2); so z + u / ln 2 overestimates sp2 by at most
+// C u^2, C = 1 / (2 ln 2), and never by more than that.  For z < 0 the same
+// expression (u = 2^z) stays below 1 / ln 2 < 1.5, so on a row whose threshold
+// theta is at least 1.5 those columns get weight 0, as they do exactly
+// (sp2(z) < 1 <= theta).  The weight of a column above the threshold with
+// exact value y = (sp2(z) - theta) kappa in (0, 1] then moves by at most
+// p min(1, y + eta)^(p-1) C kappa u^2, where u <= 2^-(theta + y/kappa - 1)
+// (because sp2(z) <= z + 1) and eta = C kappa 2^(-2 (theta - 1)) bounds the
+// overestimate; the largest value of that bound over y is taken at
+// y* = min(1, (p - 1) kappa / (2 ln 2)).  Columns below the threshold with
+// z >= 0 get at most (C kappa)^p.  With at most i columns and a row maximum
+// weight of 1 (so sum_j w_j >= 1), the row's weights change in sum by at most
+//   R = i p C kappa 2^(2 eta / kappa) y*^(p-1) 2^(-2 (theta + y*/kappa - 1)) + i (C kappa)^p
+// relative to their total.  A row takes the one-exponential weights when
+// R <= kFastBound; the output then moves by at most 2 R max_j |v_j|.
+constexpr float kFastBound = 2e-4f;
+constexpr float kHalfInvLn2 = 0.72134752044448170f;   // 1 / (2 ln 2)
+
+__device__ __forceinline__ bool fast_weights_ok(float theta, float kappa, float fi, int p) {
+    if (!(theta >= 1.5f) || p < 4) return false;
+    const float ys = fminf(1.f, (float)(p - 1) * kappa * kHalfInvLn2);
+    const float two_eta_k = 2.f * kHalfInvLn2 * ptx::ex2(-2.f * (theta - 1.f));   // 2 eta / kappa
+    const float l_i = ptx::lg2(fi);
+    const float l_r = l_i + ptx::lg2((float)p * kHalfInvLn2 * kappa) + two_eta_k + (float)(p - 1) * ptx::lg2(ys) -
+                      2.f * (theta + ys / kappa - 1.f);
+    const float l_c = l_i + (float)p * ptx::lg2(kHalfInvLn2 * kappa);
+    return ptx::ex2(l_r) + ptx::ex2(l_c) <= kFastBound;
+}
+
+// One-exponential LSSAR weights of one chunk of z (rows whose bound holds):
+// w = sat((z + u / ln 2) kappa + beta)^p with u = 2^-|z|.
+template <int PK>
+__device__ __forceinline__ void weights_fast_z(const uint32_t (&r)[32], const RowConst &rc, int p,
+                                               float2 &acc, uint32_t *pk) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float2 z = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+        const float2 u = make_float2(ptx::ex2(-fabsf(z.x)), ptx::ex2(-fabsf(z.y)));
+        const float2 t = __ffma2_rn(z, make_float2(rc.kappa, rc.kappa), make_float2(rc.beta, rc.beta));
+        const float2 w = powk2<PK>(ptx::fma_sat2(u, make_float2(rc.ck, rc.ck), t), p);
+        acc = __fadd2_rn(acc, w);
+        pk[j / 2] = ptx::pack_bf16x2(w.x, w.y);
+    }
+}
 
 // Scores of one 32-column chunk to z in place: z = a * s for the softmax
 // normalisers (raw q, k); the normalised modes' query rows already carry the
@@ -806,7 +856,9 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             rc.kappa = 0.f;
             rc.beta = 0.f;
             rc.m = 0.f;
+            rc.ck = 0.f;
             rc.uniform = false;
+            rc.fast = false;
             if constexpr (kTwoPass) {
                 float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 constexpr float kInit = MODE == kSigmoidRw ? INFINITY : -INFINITY;
@@ -907,6 +959,10 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     if (den > kDegenerateRel * spm + kDegenerateAbs) {
                         rc.kappa = 1.f / den;
                         rc.beta = -theta * rc.kappa;
+                        if constexpr (PK == 15 || PK == 0) {
+                            rc.ck = 2.f * kHalfInvLn2 * rc.kappa;
+                            rc.fast = !prm.exact_weights && fast_weights_ok(theta, rc.kappa, fi, p_row);
+                        }
                     } else {
                         // All-zero re-weighted row: an exactly uniform LSSA row (all sp
                         // equal), or one whose spread is below the softplus evaluation
@@ -918,7 +974,19 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     }
                 }
             }
-            // pass 2: weights into TMEM, running row sum
+            // pass 2: weights into TMEM, running row sum.  The warp takes the
+            // one-exponential LSSAR weights when every one of its rows meets
+            // the error bound (a warp-uniform choice).
+            const bool fastw = __all_sync(0xffffffffu, rc.fast);
+            auto weights = [&](const uint32_t (&r)[32], float2 &acc, uint32_t *pk) {
+                if constexpr (MODE == kLssar && (PK == 15 || PK == 0)) {
+                    if (fastw) {
+                        weights_fast_z<PK>(r, rc, p_row, acc, pk);
+                        return;
+                    }
+                }
+                weights_z<MODE, PK>(r, rc, p_row, acc, pk);
+            };
             float2 acc2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             for (int kt = 0; kt < n; ++kt) {
                 if (!(ok = wait_warp(s_full, sf_phase, kErrSFull))) break;
@@ -938,10 +1006,10 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     uint32_t pk0[16], pk1[16];
                     if (kt == qt) to_z<MODE, true>(r0, 64 * h, t, rc.a);
                     else to_z<MODE, false>(r0, 64 * h, t, rc.a);
-                    weights_z<MODE, PK>(r0, rc, p_row, acc2[0], pk0);
+                    weights(r0, acc2[0], pk0);
                     if (kt == qt) to_z<MODE, true>(r1, 64 * h + 32, t, rc.a);
                     else to_z<MODE, false>(r1, 64 * h + 32, t, rc.a);
-                    weights_z<MODE, PK>(r1, rc, p_row, acc2[1], pk1);
+                    weights(r1, acc2[1], pk1);
                     if (p_pending) {
                         if (!(ok = wait_warp(p_free, pf_phase, kErrPFree))) break;
                         pf_phase ^= 1;
@@ -961,14 +1029,14 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     uint32_t pk[16];
                     if (kt == qt) to_z<MODE, true>(r0, 64 * h, t, rc.a);
                     else to_z<MODE, false>(r0, 64 * h, t, rc.a);
-                    weights_z<MODE, PK>(r0, rc, p_row, acc2[0], pk);
+                    weights(r0, acc2[0], pk);
                     ptx::tmem_st16(p_col, pk);
                 }
                 {
                     uint32_t pk[16];
                     if (kt == qt) to_z<MODE, true>(r1, 64 * h + 32, t, rc.a);
                     else to_z<MODE, false>(r1, 64 * h + 32, t, rc.a);
-                    weights_z<MODE, PK>(r1, rc, p_row, acc2[1], pk);
+                    weights(r1, acc2[1], pk);
                     ptx::tmem_st16(p_col + 16, pk);
                 }
                 ptx::tmem_st_wait();

@@ -271,3 +271,53 @@ def test_nonzero_stream_and_preallocated_out(torch_mod):
     s.synchronize()
     ref = attention_forward(*(bf16_bits_to_f64(t) for t in (qb, kb, vb)), MODE_LSSAR, 3)
     assert np.abs(out.float().cpu().numpy() - ref).max() <= 2e-2
+
+
+def bf16_ulp(x):
+    """Spacing of bfloat16 numbers at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+@pytest.mark.parametrize("structure,p,min_moved", [("iid", 15, 0.5), ("needle", 15, 0.0), ("iid", 64, 0.2)])
+def test_one_exponential_weights(torch_mod, structure, p, min_moved, monkeypatch):
+    # LSSAR rows whose error bound holds take z + 2^-|z|/ln 2 for the softplus
+    # in the weight pass; LSSAR_EXACT_WEIGHTS=1 keeps log2(1 + 2^z) on every row.
+    # The row sums W = sum_j w_j saved by the training forward show which rows
+    # took the one-exponential weights (W differs in its low bits) and bound
+    # the change (at most 2e-4 of W); the outputs agree to within one bf16
+    # rounding step, and both match the oracle on sampled rows.
+    from lssar_attn_fwd_gb300 import api
+    torch = torch_mod
+    B, H, L, d = 1, 2, 8192, 64
+    qb, kb, vb = make_qkv(B, H, L, d, seed=5, structure=structure)
+    q, k, v = (to_dev(torch, t) for t in (qb, kb, vb))
+    monkeypatch.delenv("LSSAR_EXACT_WEIGHTS", raising=False)
+    out_f, st_f = api.lssar_attn_fwd_train(q, k, v, p=p, mode=MODE_LSSAR)
+    monkeypatch.setenv("LSSAR_EXACT_WEIGHTS", "1")
+    out_e, st_e = api.lssar_attn_fwd_train(q, k, v, p=p, mode=MODE_LSSAR)
+    monkeypatch.delenv("LSSAR_EXACT_WEIGHTS")
+    torch.cuda.synchronize()
+    of, oe = (t.float().cpu().numpy().astype(np.float64) for t in (out_f, out_e))
+    wf, we = (t.cpu().numpy()[..., 3].astype(np.float64) for t in (st_f, st_e))
+    # a row's weight sum moves by at most 2e-4 of itself, so its output by at
+    # most 2 * 2e-4 * max|v|; a weight that crosses a rounding boundary of the
+    # bf16 P fed to the tensor core moves by one bf16 step (2^-8 of itself,
+    # at most 2^-8 max|v| on the output); then one bf16 rounding of the output
+    vmax = np.abs(bf16_bits_to_f64(vb)).max()
+    diff = np.abs(of - oe) - bf16_ulp(np.maximum(np.abs(of), np.abs(oe)))
+    assert diff.max() <= (4e-4 + 2.0 ** -8) * vmax, (diff.max(), np.abs(of - oe).max())
+    rel = np.abs(wf - we) / we
+    assert rel.max() <= 2e-4, rel.max()
+    moved = wf != we
+    assert not moved[..., :3].any()          # rows 1-3 (O = 0) keep the exact weights
+    # W moves on most iid rows at p = 15; where one weight dominates (the
+    # needle rows, p = 64) W is that weight plus terms below its fp32
+    # rounding step, so it moves on fewer rows
+    assert moved.mean() > min_moved, moved.mean()
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    rows = sample_rows(L, seed=6)
+    for h in range(H):
+        ref = attention_forward(qf[0, h], kf[0, h], vf[0, h], MODE_LSSAR, p, rows=rows)
+        assert np.abs(of[0, h, rows - 1] - ref).max() <= tol(MODE_LSSAR, p)
+    check_error_word()
