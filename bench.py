@@ -38,6 +38,8 @@ REWEIGHT_MODES = (MODE_LSSAR, MODE_SOFTMAX_RW, MODE_SIGMOID_RW)
 FLUSH_BYTES = 256 << 20
 L2_BYTES = 129 << 20   # GB300 L2
 FALLBACK_BF16_TFLOPS = 1900.0
+SPEC_DENSE_BF16_TFLOPS = 2250.0   # GB300 nominal dense bf16 tensor peak (context beside the measured one)
+MIN_LOAD_S = 0.6                  # seconds of the same step under load for the clock record
 
 
 def gemm_count(mode):
@@ -96,11 +98,15 @@ def kernel_traffic(workload, mode, p):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons, 50 ms apart."""
+    """nvidia-smi samples of SM clock, utilisation and throttle reasons: a
+    background poll 50 ms apart, plus synchronous single queries (taken at
+    both ends of the timed region, so that even a region shorter than the
+    poll interval has clock evidence)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
 
     def __init__(self, index):
         self.samples = []
@@ -122,6 +128,16 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
 
+    def query_once(self):
+        """One synchronous sample, stamped with the time the query returned."""
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+            line = r.stdout.strip().splitlines()[0]
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+        except Exception:
+            pass
+
     def stop(self):
         if self.proc is not None:
             self.proc.terminate()
@@ -130,25 +146,39 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
-        win = [s for (t, s) in self.samples if t0 <= t <= t1 and len(s) >= 8]
+    def summary(self, t0, t1, timed=None):
+        """Clock record over the load window [t0, t1] (the same step running
+        back to back: warm-up, timed region, untimed repeats); `timed` =
+        (w0, w1) also reports the samples inside the timed region itself (the
+        synchronous queries at its two ends fall on its edges)."""
+        win = [(t, s) for (t, s) in self.samples if t0 <= t <= t1 and len(s) >= 8]
         if not win:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_under_load": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in win for i in range(4) if s[4 + i].lower().startswith("active")})
 
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(s[0]) for s in win if num(s[0]) is not None]
-        mx = [num(s[1]) for s in win if num(s[1]) is not None]
-        pw = [num(s[2]) for s in win if num(s[2]) is not None]
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None,
-                "reasons": reasons, "samples": len(win)}
+        loaded = [s for _, s in win if len(s) < 9 or (num(s[8]) is not None and num(s[8]) >= 50.0)]
+        use = loaded or [s for _, s in win]
+        reasons = sorted({names[i] for s in use for i in range(4) if s[4 + i].lower().startswith("active")})
+        sm = [num(s[0]) for s in use if num(s[0]) is not None]
+        mx = [num(s[1]) for _, s in win if num(s[1]) is not None]
+        pw = [num(s[2]) for s in use if num(s[2]) is not None]
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None,
+               "power_w_max": max(pw) if pw else None,
+               "reasons": reasons, "samples": len(win), "samples_under_load": len(loaded),
+               "window_s": round(t1 - t0, 3)}
+        if timed is not None:
+            w0, w1 = timed
+            tw = [s for (t, s) in win if w0 - 0.05 <= t <= w1 + 0.05]
+            tsm = [num(s[0]) for s in tw if num(s[0]) is not None]
+            out["samples_timed"] = len(tw)
+            out["sm_mhz_timed"] = statistics.median(tsm) if tsm else None
+        return out
 
 
 def reduce_max_over_ranks(values, device):
@@ -286,15 +316,18 @@ def run_ours(args, wl, mode, p):
     for trio in ev:
         for e in trio:
             e.record(stream)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.2)
+    load0 = time.time()
     for _ in range(W):
         flush.zero_()
         api.lssar_attn_fwd(q, k, v, p=p, mode=mode, out=out)
     torch.cuda.synchronize(dev)
 
-    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
     if sampler:
-        sampler.start()
-        time.sleep(0.3)
+        sampler.query_once()
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -306,6 +339,8 @@ def run_ours(args, wl, mode, p):
     if ws > 1:
         dist.barrier()
     w1 = time.time()
+    if sampler:
+        sampler.query_once()
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
     kern_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     tot, kern_mean = reduce_max_over_ranks([sum(step_ms), sum(kern_ms) / K], dev)
@@ -379,8 +414,18 @@ def run_ours(args, wl, mode, p):
         e1.record(stream)
         torch.cuda.synchronize(dev)
     serial_ms = reduce_max_over_ranks([e0.elapsed_time(e1) / KE], dev)[0]
+    # untimed repeats of the timed step (same flush, same call) until the GPU
+    # has run this load for MIN_LOAD_S, so that the clock record has samples
+    # under load even when the timed region is shorter than the poll interval
+    while time.time() - load0 < MIN_LOAD_S:
+        for _ in range(20):
+            flush.zero_()
+            api.lssar_attn_fwd(q, k, v, p=p, mode=mode, out=out)
+        torch.cuda.synchronize(dev)
+    load1 = time.time()
     if sampler:
-        time.sleep(0.2)
+        sampler.query_once()
+        time.sleep(0.1)
         sampler.stop()
 
     if rank == 0:
@@ -400,8 +445,10 @@ def run_ours(args, wl, mode, p):
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": config_dict(wl, mode, p),
             "pct_bf16_peak": 100.0 * value / ws / peak,
+            "pct_bf16_spec_peak": 100.0 * value / ws / SPEC_DENSE_BF16_TFLOPS,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                         "frac_of_spec_dense_bf16": achieved / SPEC_DENSE_BF16_TFLOPS,
                          "kernel": "lssar_tc_kernel", "kernel_ms": kern_mean,
                          "kernel_ms_median": kern_median,
                          "traffic": kernel_traffic(wl.name, mode, p)},
@@ -416,7 +463,7 @@ def run_ours(args, wl, mode, p):
                                "note": "copies and kernel back to back on one stream"},
                     "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2},
             "gpu_launches": K * launches_per_step,
-            "clocks": sampler.summary(w0, w1) if sampler else None,
+            "clocks": sampler.summary(load0, load1, timed=(w0, w1)) if sampler else None,
             "wall_s_timed": w1 - w0,
             "cpu_baseline": cpu,
         }
@@ -454,6 +501,7 @@ def run_decode(args, mode, p):
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     torch.cuda.synchronize()
+    sampler.query_once()
     t0 = time.time()
     for a, b in ev:
         if flush_each:
@@ -463,6 +511,7 @@ def run_decode(args, mode, p):
         b.record(s)
     torch.cuda.synchronize()
     t1 = time.time()
+    sampler.query_once()
     sampler.stop()
     ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
     gbs = cache_bytes / (ms * 1e-3) / 1e9
@@ -480,7 +529,7 @@ def run_decode(args, mode, p):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": f"{kind} hbm_gbs"},
         "plan": plan,
-        "clocks": sampler.summary(t0, t1),
+        "clocks": sampler.summary(t0 - 1.0, t1 + 1.0, timed=(t0, t1)),
         "gpu_launches": plan["launches"] * args.steps}), flush=True)
 
 
@@ -511,6 +560,7 @@ def run_backward(args, wl, mode, p):
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     torch.cuda.synchronize()
+    sampler.query_once()
     t0 = time.time()
     for a, b in ev:
         flush.zero_()
@@ -519,6 +569,7 @@ def run_backward(args, wl, mode, p):
         b.record(s)
     torch.cuda.synchronize()
     t1 = time.time()
+    sampler.query_once()
     sampler.stop()
     assert api.device_error_word() == 0
     ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
@@ -534,7 +585,7 @@ def run_backward(args, wl, mode, p):
                    "l2": "flushed before every step (256 MiB write)"},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "peak_source": f"{kind} bf16_tflops (burst)"},
-        "clocks": sampler.summary(t0, t1),
+        "clocks": sampler.summary(t0 - 1.0, t1 + 1.0, timed=(t0, t1)),
         "gpu_launches": (4 if uses_normalised(mode) else 3) * args.steps}), flush=True)
 
 

@@ -31,6 +31,11 @@
  *     by the library and released stream-ordered on the same stream.
  *   - Thread-safe: no mutable global state besides the lazily created pool
  *     (guarded) and the device error word (see lssar_device_error_word).
+ *   - The device addresses of the library's own device variables (the error
+ *     word, the fixed scratch of lssar_attn_fwd_noalloc) and its memory pool
+ *     are looked up once per device and kept: after cudaDeviceReset (or any
+ *     other teardown of a device's primary context) the library must not be
+ *     used on that device again in the same process.
  */
 #ifndef LSSAR_ATTN_FWD_H
 #define LSSAR_ATTN_FWD_H
@@ -221,8 +226,8 @@ int lssar_attn_fwd_profiled(const void *q, const void *k, const void *v, void *o
  *
  * Same operation, arguments and results as lssar_attn_fwd.  The caller still
  * provides q, k, v and out; the temporary data (a work counter and the
- * normalised q and k in fp16, 256 + 4*B*H*L*d bytes in LSSA/LSSAR mode, 256
- * bytes in softmax mode) lives in one fixed device array of
+ * normalised q and k in fp16: 256 + 2*round_up(2*B*H*L*d, 256) bytes in
+ * LSSA/LSSAR mode, 256 bytes in softmax mode) lives in one fixed device array of
  * LSSAR_NOALLOC_SCRATCH_BYTES compiled into the library.  Problems that need
  * more return LSSAR_ERR_SCRATCH before anything is launched (for example
  * B*H*L*d must stay below about 8.4 million elements in LSSA/LSSAR mode).
@@ -234,7 +239,10 @@ int lssar_attn_fwd_profiled(const void *q, const void *k, const void *v, void *o
  * and it keeps the previous call's contents; the parts that must start at zero
  * are cleared by each call on its stream.  Calls whose execution overlaps on
  * the GPU (different streams, or different host threads, without ordering
- * between them) race on the array: order them.
+ * between them) race on the array: order them.  The device address of the
+ * array is looked up once per device and kept: do not use the library on a
+ * device after cudaDeviceReset (or any other teardown of its primary context)
+ * in the same process.
  */
 int lssar_attn_fwd_noalloc(const void *q, const void *k, const void *v, void *out,
                            int B, int H, int L, int d, int p, int mode, cudaStream_t stream);

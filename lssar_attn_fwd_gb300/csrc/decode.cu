@@ -346,7 +346,7 @@ __device__ void weights_from_stats(float2 hs, int L, int mode, int p, const floa
         const float theta = o * s1 / (float)L;
         const float top = phi(mode, m, m);   // the normaliser at the row maximum
         const float den = top - theta;
-        if (den > 1e-4f * top + 1e-6f) {
+        if (den > 1e-5f * top + 2e-5f) {   // the prefill kernel's near-uniform band
             kappa = 1.f / den;
             beta = -theta * kappa;
         } else {

@@ -275,12 +275,23 @@ __device__ __forceinline__ float2 powk2(float2 r, int p) {
     }
 }
 
-// A re-weighted row counts as all-zero when sp2(m) - theta is within the
-// evaluation error of sp2 (relative ~1e-6 from the MUFU approximations, and
-// the two passes evaluate it by different formulas; absolute 1e-7 where
-// 1 + 2^z rounds to 1): the spread of such a row cannot be resolved in fp32.
-constexpr float kDegenerateRel = 1e-4f;
-constexpr float kDegenerateAbs = 1e-6f;
+// A re-weighted row counts as all-zero when sp2(m) - theta is within a few
+// times the evaluation error of sp2 in pass 2: its weights would then follow
+// that error rather than the scores.  Pass 2 evaluates sp2 of different
+// columns by different formulas (MUFU ex2 and lg2: about 2.4e-7 of the value;
+// the polynomial log2: up to 2.2e-6 absolute), and pass 1 sums it in product
+// form, so columns with equal scores can differ by about 2.5e-6 + 2.4e-7 sp2.
+// The band is 1e-5 sp2(m) + 2e-5: about 40 times the relative and 8 times
+// the absolute part.
+constexpr float kDegenerateRel = 1e-5f;
+constexpr float kDegenerateAbs = 2e-5f;
+// Weights of such a row: the saturating FMA sat(phi * 2^126 + 0) is exactly 1
+// for every column whose normaliser value phi (softplus, 2^(z - m), sigmoid)
+// is positive in fp32 and exactly 0 on the masked columns above the diagonal
+// (phi = 0 there), so the output is the prefix mean.  (Columns whose softplus
+// rounds to 0 in fp32, scores below -24 on the two-transcendental path, also
+// get 0; a row read as uniform has them only if every score is below -24.)
+constexpr float kUniformSlope = 8.507059e37f;   // 2^126
 
 struct RowConst {
     float a;       // score scale: z = a * s
@@ -932,7 +943,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         rc.kappa = 1.f / den;
                         rc.beta = -theta * rc.kappa;
                     } else {
-                        rc.kappa = 1.f;   // all-zero re-weighted row: (2^(z-m))^p ~= 1
+                        rc.kappa = kUniformSlope;   // all-zero re-weighted row (see kUniformSlope)
                         rc.beta = 0.f;
                         rc.uniform = true;
                     }
@@ -946,7 +957,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         rc.kappa = 1.f / den;
                         rc.beta = -theta * rc.kappa;
                     } else {
-                        rc.kappa = 1.f / sgm;   // all-zero re-weighted row
+                        rc.kappa = kUniformSlope;   // all-zero re-weighted row (see kUniformSlope)
                         rc.beta = 0.f;
                         rc.uniform = true;
                     }
@@ -965,10 +976,9 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         }
                     } else {
                         // All-zero re-weighted row: an exactly uniform LSSA row (all sp
-                        // equal), or one whose spread is below the softplus evaluation
-                        // error; (sp / sp_max)^p ~= 1 on every unmasked column gives the
-                        // uniform prefix mean.
-                        rc.kappa = 1.f / spm;
+                        // equal), or one whose spread is within the band above
+                        // (see kUniformSlope for its weights).
+                        rc.kappa = kUniformSlope;
                         rc.beta = 0.f;
                         rc.uniform = true;
                     }

@@ -16,6 +16,13 @@ pages' datasets are not used):
 iid inputs: ``numpy.random.default_rng(seed)`` draws q, then k, then v as
 float32 N(0, 1) and rounds each to bf16 (round to nearest even).
 
+odd_key inputs (near-uniform rows): the generator draws q (float32 N(0,1),
+rounded to bf16), then one key k0 per head and v, then per head a component
+c uniform on 0..d-1.  Every key of the head is k0 except key 2 (1-based),
+whose component c is moved away from zero by ``odd_ulps`` bf16 steps (its bit
+pattern plus odd_ulps).  Each row then holds i-1 equal keys and one slightly
+different one, so its LSSA row is uniform up to a small controlled spread.
+
 needle inputs: the same generator draws k, then v (float32 N(0,1), rounded
 to bf16), then j(i) uniform on the integers 1..i for every row i (1-based),
 then noise ~ N(0, I/d) as float32.  Query i is
@@ -80,10 +87,20 @@ def bf16_bits_to_f64(b):
     return bf16_bits_to_f32(b).astype(np.float64)
 
 
-def make_qkv(B, H, L, d, seed=0, structure="iid"):
+def make_qkv(B, H, L, d, seed=0, structure="iid", odd_ulps=1):
     """Seeded q, k, v as uint16 bf16 bit arrays of shape [B, H, L, d]."""
     rng = np.random.default_rng(seed)
     shape = (B, H, L, d)
+    if structure == "odd_key":
+        q = f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+        k0 = f32_to_bf16_bits(rng.standard_normal((B, H, d), dtype=np.float32))
+        v = f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+        c = rng.integers(0, d, size=(B, H))
+        k = np.repeat(k0[:, :, None, :], L, axis=2).copy()
+        if L >= 2:
+            bi, hi = np.meshgrid(np.arange(B), np.arange(H), indexing="ij")
+            k[bi, hi, 1, c] = (k0[bi, hi, c].astype(np.int64) + int(odd_ulps)).astype(np.uint16)
+        return q, k, v
     if structure == "iid":
         q = f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
         k = f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))

@@ -33,4 +33,10 @@ def test_forward_bench_line_has_the_contract_keys():
         assert key in e2e, key
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 2 * d["steps"]   # prologue + attention kernel per step
-    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+    assert {"sm_mhz", "sm_max_mhz", "reasons", "samples", "samples_under_load", "samples_timed"} <= set(d["clocks"])
+    # a 5-step timed region is far shorter than the 50 ms poll: the clock
+    # record still has samples (the synchronous queries at both ends of the
+    # timed region and the untimed repeats of the same step) and a clock
+    assert d["clocks"]["samples"] >= 2 and d["clocks"]["samples_timed"] >= 2
+    assert d["clocks"]["samples_under_load"] >= 1 and d["clocks"]["sm_mhz"] is not None
+    assert abs(d["pct_bf16_spec_peak"] - 100.0 * d["value"] / 2250.0) < 1e-6

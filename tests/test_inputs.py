@@ -63,3 +63,21 @@ def test_workload_table():
     assert WORKLOADS["extrap"].shape == (1, 12, 8192, 64)
     assert WORKLOADS["needle"].structure == "needle"
     assert WORKLOADS["wide"].d == 128
+
+
+@pytest.mark.parametrize("ulps", [1, 16])
+def test_odd_key_structure(ulps):
+    q, k, v = make_qkv(2, 3, 40, 64, seed=7, structure="odd_key", odd_ulps=ulps)
+    assert q.shape == k.shape == v.shape == (2, 3, 40, 64)
+    for b in range(2):
+        for h in range(3):
+            kh = k[b, h]
+            # every key equals key 1 except key 2, which differs in one component
+            assert (kh[2:] == kh[0]).all()
+            diff = np.nonzero(kh[1] != kh[0])[0]
+            assert diff.size == 1
+            c = diff[0]
+            assert int(kh[1, c]) - int(kh[0, c]) == ulps      # bit pattern moved by `ulps` steps
+            assert abs(bf16_bits_to_f64(kh[1, c])) > abs(bf16_bits_to_f64(kh[0, c]))   # away from zero
+    a = make_qkv(2, 3, 40, 64, seed=7, structure="odd_key", odd_ulps=ulps)
+    assert all((x == y).all() for x, y in zip(a, (q, k, v)))

@@ -321,3 +321,78 @@ def test_one_exponential_weights(torch_mod, structure, p, min_moved, monkeypatch
         ref = attention_forward(qf[0, h], kf[0, h], vf[0, h], MODE_LSSAR, p, rows=rows)
         assert np.abs(of[0, h, rows - 1] - ref).max() <= tol(MODE_LSSAR, p)
     check_error_word()
+
+
+@pytest.mark.parametrize("odd_ulps", [1, 4, 16, 64])
+@pytest.mark.parametrize("p", [3, 15])
+def test_near_uniform_rows(torch_mod, odd_ulps, p):
+    # Rows of i-1 equal keys and one key that differs by odd_ulps bf16 steps in
+    # one component: the LSSA row is uniform up to a small spread, and Key
+    # design 2 then puts all weight on the odd key (if it scores higher) or
+    # spreads it evenly over the equal keys.  The kernel reads a row as the
+    # 0/0 (prefix-mean) row when sp2(m) - theta <= 1e-4 sp2(m) + 1e-6.
+    #
+    # What the fp16 score operands can resolve: rounding q and k to fp16 moves
+    # the score difference dz of the odd key and the others by at most
+    # 2^-11 a_i (a_i = log2(e) ln d ln i; Cauchy-Schwarz on the rounding
+    # errors).  What the fp32 softplus can resolve: for z >= 0 it is accurate
+    # to about 1e-6 of its value, but for z < 0 (softplus below 1) the
+    # MUFU lg2 near 1 and the product-form sum leave about 1e-4 of it, which
+    # a near-uniform row (tiny sp2(m) - theta) amplifies.  Rows whose |dz|
+    # exceeds twice the fp16 bound and whose largest score is >= 0 are decided
+    # the same way in the kernel as in exact arithmetic and must match the
+    # oracle element by element.
+    # Rows the kernel flags as uniform (read back from the training statistics:
+    # kappa = 0) must return the prefix mean, and must be within the fp16
+    # resolution of uniform; no row far from uniform may be flagged.  Every
+    # row's output is a convex combination of the values.
+    from lssar_attn_fwd_gb300 import api
+    from oracle import l2_normalize_rows, lssa_rows
+    torch = torch_mod
+    B, H, L, d = 1, 2, 512, 64
+    qb, kb, vb = make_qkv(B, H, L, d, seed=odd_ulps, structure="odd_key", odd_ulps=odd_ulps)
+    q, k, v = (to_dev(torch, t) for t in (qb, kb, vb))
+    out, st = api.lssar_attn_fwd_train(q, k, v, p=p, mode=MODE_LSSAR)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy().astype(np.float64)
+    flagged = st.cpu().numpy()[..., 1] == 0.0            # kappa = 0: read as uniform
+    qf, kf, vf = (bf16_bits_to_f64(t) for t in (qb, kb, vb))
+    rows = np.arange(1, L + 1)
+    decided = flagged_rows = 0
+    for h in range(H):
+        ref = attention_forward(qf[0, h], kf[0, h], vf[0, h], MODE_LSSAR, p)
+        a = lssa_rows(qf[0, h], kf[0, h], rows, d)
+        den_rel = (a.max(1) - 1.0 / rows) / a.max(1)
+        ai = np.log(d) * np.log(rows) / np.log(2.0)
+        qh, kh = l2_normalize_rows(qf[0, h]), l2_normalize_rows(kf[0, h])
+        dz = ai * (qh @ (kh[1] - kh[0]))                  # odd key minus the equal keys, log2 units
+        zmax = ai * np.maximum(qh @ kh[0], np.where(rows >= 2, qh @ kh[1], -np.inf))
+        sure = (np.abs(dz) > 2.0 * 2.0 ** -11 * ai) & (zmax >= 0.0)
+        sure[0] = True                                    # row 1 attends one key only
+        e = np.abs(got[0, h] - ref).max(1)
+        assert (e[sure] <= tol(MODE_LSSAR, p)).all(), (e[sure].max(), rows[sure][e[sure].argmax()])
+        fl = flagged[0, h]
+        fl[:3] = False                                    # rows 1-3 have O = 0: no threshold
+        pm = np.cumsum(vf[0, h], axis=0) / rows[:, None]
+        assert (np.abs(got[0, h, fl] - pm[fl]).max(initial=0.0) <= 2e-2)
+        # a row whose odd key scores higher by more than the fp16 resolution
+        # has sp2(m) - theta of at least about 2^-10 a_i sigma(z) (i-1)/i,
+        # far above the band: the kernel never flags it.  (When the odd key
+        # scores lower, sp2(m) - theta = (sp2(z_a) - sp2(z_b)) / i can fall in
+        # the band; the exact answer, the mean over the equal keys, is then
+        # within |v| / (i - 1) of the prefix mean and the parity check above
+        # covers it.)
+        assert not (fl & sure & (dz > 0)).any()
+        cummin = np.minimum.accumulate(vf[0, h], axis=0)
+        cummax = np.maximum.accumulate(vf[0, h], axis=0)
+        assert (got[0, h] >= cummin - 2e-2).all() and (got[0, h] <= cummax + 2e-2).all()
+        decided += int(sure.sum())
+        flagged_rows += int(fl.sum())
+    # the sweep spans the band: perturbations of 1 and 4 bf16 steps stay below
+    # the fp16 resolution on every row (and reach the band on many), those of
+    # 16 and 64 steps are resolved on most rows
+    if odd_ulps >= 16:
+        assert decided >= 50, decided
+    else:
+        assert flagged_rows >= 10, flagged_rows
+    check_error_word()

@@ -39,13 +39,16 @@ def test_rejects_problems_beyond_the_fixed_scratch(lib):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("shape,mode,p,tol", [
-    ((1, 12, 1024, 64), MODE_LSSAR, 15, 5e-2),
-    ((2, 4, 700, 128), MODE_LSSAR, 3, 2e-2),
-    ((1, 2, 300, 64), MODE_LSSA, 1, 2e-2),
-    ((2, 3, 257, 64), MODE_SOFTMAX, 1, 2e-2),
+@pytest.mark.parametrize("shape,mode,p", [
+    ((1, 12, 1024, 64), MODE_LSSAR, 15),
+    ((2, 4, 700, 128), MODE_LSSAR, 3),
+    ((1, 2, 300, 64), MODE_LSSA, 1),
+    ((2, 3, 257, 64), MODE_SOFTMAX, 1),
 ])
-def test_matches_default_entry_point_on_two_calls(lib, shape, mode, p, tol):
+def test_matches_default_entry_point_on_two_calls(lib, shape, mode, p):
+    # Both entry points run the same deterministic kernels on the same inputs
+    # (only where the scratch lives differs), so the outputs must agree bit
+    # for bit; a stale or shifted scratch would show up as any difference.
     import torch
     from lssar_attn_fwd_gb300 import api
     qb, kb, vb = make_qkv(*shape, seed=11)
@@ -59,6 +62,5 @@ def test_matches_default_entry_point_on_two_calls(lib, shape, mode, p, tol):
                           out.data_ptr(), *shape, p, mode, stream)
         assert st == 0, api.status_string(st)
         torch.cuda.synchronize()
-        err = (out.float() - ref.float()).abs().max().item()
-        assert err <= tol, err
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert api.device_error_word() == 0
