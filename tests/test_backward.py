@@ -5,21 +5,29 @@ The training forward (lssar_attn_fwd_train) must give exactly the output of
 lssar_attn_fwd and row statistics consistent with the oracle; the backward
 (dq, dk, dv in bf16) must match the oracle's gradients element by element.
 
-Tolerance, per gradient tensor (TOL = 2e-2, or 5e-2 for p >= 15 in the
-re-weighting modes, as for the forward's output):
-  aggregate     ||got - ref||_2 <= TOL * ||ref||_2 + 1e-3 * sqrt(n)
-  elementwise   max |got - ref| <= 3 TOL * max |ref| + 1e-3
-The scores are products of fp16-rounded normalised rows (as in the forward),
-and a row's weights respond to a score error with a gain of about p * kappa_i:
-in a nearly uniform short row (kappa_i large, e.g. row 4 with kappa = 15.75)
-that gain turns the fp16 rounding alone into a few per cent of that row's
-gradient -- an exact-arithmetic emulation with only q, k rounded to fp16 gives
-the same error.  Such rows are kept out of the comparison by a zero upstream
-gradient (well_conditioned_dout, decided from the oracle alone).  At p = 1 the
-gradient also jumps at the ReLU kink, where entries within the score error
-of the kink may fall on either side; the elementwise bound covers them, the
-aggregate bound holds the tensor as a whole to the forward's tolerance.  The
-bf16 rounding of the gradients adds 2^-9 relative.
+Tolerance, per gradient tensor, with TOL = 2e-2, or 5e-2 for p >= 15 in
+the re-weighting modes (the forward's tolerance):
+  elementwise   |got_ic - ref_ic| <= TOL (max_c' |ref_ic'| + 1e-2 G) + 2^-8 |ref_ic| + 1e-4
+  aggregate     ||got - ref||_2 <= TOL ||ref||_2 + 1e-3 sqrt(n)
+i.e. each element against its own row's largest gradient (a row's elements
+are sums over the same weights and score gradients, and the kernel's errors
+are relative to those), with a floor of 1 % of G, the largest entry of the
+three gradients, for rows whose gradient cancels to near zero (a row of equal
+keys has dq = 0 exactly, and the fp16 score gradients leave residues of about
+2^-11 of their own size), plus 2^-8 for the bf16 rounding of
+the result (1e-4: rounding residues where the exact gradient is 0).  Measured on this GPU, the largest error over all these cases is
+0.017 of that scale (LSSAR p = 3: 0.014).  At p = 1 the re-weighting's ReLU has
+a kink: a weight whose score lies within the score error of it may fall on
+the other side, which moves that row by its whole contribution at the kink;
+for p = 1 the elementwise bound is 3 TOL max |ref| (measured: 0.027 max |ref|).
+
+Rows whose re-weighting is ill-conditioned at the precision of the fp16
+score operands (well_conditioned_dout: a row's weights respond to a score
+error with a gain of about p * kappa_i, and in a nearly uniform short row
+that gain turns the fp16 rounding alone into a few per cent of its gradient)
+get a zero upstream gradient on both sides.  The tests assert how many rows
+that drops: at most 1 % of the rows (and one row in the smallest cases); the
+seeded inputs here drop at most 2 rows of 256.
 """
 
 import numpy as np
@@ -55,6 +63,9 @@ def to_dev(torch, bits):
 
 def to_np(t):
     return t.float().cpu().numpy().astype(np.float64)
+
+
+MAX_DROPPED = 0.01   # largest fraction of rows well_conditioned_dout may drop
 
 
 def well_conditioned_dout(qb, kb, db, mode, p, limit=0.02):
@@ -95,10 +106,19 @@ def well_conditioned_dout(qb, kb, db, mode, p, limit=0.02):
     return out
 
 
+def reference(qb, kb, vb, db, mode, p):
+    return attention_backward(*(bf16_bits_to_f64(t) for t in (qb, kb, vb, db)), mode, p)
+
+
 def run_backward(torch, B, H, L, d, mode, p, seed, impl="simt"):
     from lssar_attn_fwd_gb300 import api
     qb, kb, vb = make_qkv(B, H, L, d, seed=seed)
-    db = well_conditioned_dout(qb, kb, make_dout(B, H, L, d, seed=seed), mode, p)
+    d0 = make_dout(B, H, L, d, seed=seed)
+    db = well_conditioned_dout(qb, kb, d0, mode, p)
+    dropped = int((np.any(db != d0, axis=-1)).sum())
+    rows = B * H * L
+    print(f"well-conditioned rows: {rows - dropped} of {rows} kept (mode {mode}, p {p}, L {L}, d {d})")
+    assert dropped <= max(1, MAX_DROPPED * rows), (dropped, rows)
     q, k, v, dout = (to_dev(torch, t) for t in (qb, kb, vb, db))
     out, stats = api.lssar_attn_fwd_train(q, k, v, p=p, mode=mode)
     fn = api.lssar_attn_bwd_simt if impl == "simt" else api.lssar_attn_bwd
@@ -106,18 +126,24 @@ def run_backward(torch, B, H, L, d, mode, p, seed, impl="simt"):
     torch.cuda.synchronize()
     assert api.device_error_word() == 0
     got = tuple(to_np(t) for t in (dq, dk, dv))
-    ref = attention_backward(*(bf16_bits_to_f64(t) for t in (qb, kb, vb, db)), mode, p)
-    return got, ref
+    return got, reference(qb, kb, vb, db, mode, p)
 
 
 def assert_close(got, ref, mode, p, what=""):
     t = tol(mode, p)
+    kink = mode in RW_MODES and p == 1
+    top_all = max(float(np.abs(r).max()) for r in ref)   # the problem's gradient scale
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
-        scale = float(np.abs(r).max())
-        err = float(np.abs(g - r).max())
         fro, nrm = float(np.linalg.norm(g - r)), float(np.linalg.norm(r))
         assert fro <= t * nrm + 1e-3 * np.sqrt(r.size), f"{what} {name}: ||err|| {fro:.3e} ||ref|| {nrm:.3e}"
-        assert err <= 3 * t * scale + 1e-3, f"{what} {name}: err {err:.3e} scale {scale:.3e}"
+        top = float(np.abs(r).max())
+        if kink:
+            bound = 3 * t * top + 1e-3 + 0.0 * r
+        else:
+            bound = t * (np.abs(r).max(axis=-1, keepdims=True) + 1e-2 * top_all) + 2.0 ** -8 * np.abs(r) + 1e-4
+        excess = np.abs(g - r) - bound
+        assert excess.max() <= 0.0, (f"{what} {name}: |err| {np.abs(g - r).flat[excess.argmax()]:.3e} "
+                                     f"over the bound {bound.flat[excess.argmax()]:.3e}")
 
 
 MODES = [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_LSSAR, 1), (MODE_LSSA, 1), (MODE_SOFTMAX, 1),
@@ -183,7 +209,7 @@ def test_backward_simt_uniform_rows(torch_mod):
     st = stats.cpu().numpy()
     assert np.all(st[0, 0, 3:, 1] == 0.0) and np.all(st[0, 0, 3:, 2] == 1.0)
     np.testing.assert_array_equal(st[0, 0, 3:, 3], np.arange(4, L + 1, dtype=np.float32))
-    ref = attention_backward(*(bf16_bits_to_f64(t) for t in (qb, kb, vb, db)), MODE_LSSAR, 3)
+    ref = reference(qb, kb, vb, db, MODE_LSSAR, 3)
     assert np.abs(to_np(dq)[0, 0, 3:]).max() == 0.0
     assert_close((to_np(dq), to_np(dk), to_np(dv)), ref, MODE_LSSAR, 3)
 
@@ -226,8 +252,7 @@ def test_backward_tc_many_items(torch_mod):
         a, b = to_np(a), to_np(b)
         assert np.abs(a - b).max() <= 2e-2 * np.abs(b).max()
     for bb, hh in ((0, 0), (1, 79)):
-        ref = attention_backward(*(bf16_bits_to_f64(t[bb:bb + 1, hh:hh + 1]) for t in (qb, kb, vb, db)),
-                                 MODE_LSSAR, p)
+        ref = reference(*(t[bb:bb + 1, hh:hh + 1] for t in (qb, kb, vb, db)), MODE_LSSAR, p)
         assert_close(tuple(to_np(t)[bb:bb + 1, hh:hh + 1] for t in tc), ref, MODE_LSSAR, p)
 
 
@@ -263,6 +288,6 @@ def test_backward_tc_uniform_rows(torch_mod):
     dq, dk, dv = api.lssar_attn_bwd(q, k, v, dout, stats, p=15, mode=MODE_LSSAR)
     torch.cuda.synchronize()
     assert api.device_error_word() == 0
-    ref = attention_backward(*(bf16_bits_to_f64(t) for t in (qb, kb, vb, db)), MODE_LSSAR, 15)
+    ref = reference(qb, kb, vb, db, MODE_LSSAR, 15)
     assert np.abs(to_np(dq)[0, 0, 3:]).max() == 0.0
     assert_close((to_np(dq), to_np(dk), to_np(dv)), ref, MODE_LSSAR, 15)
