@@ -13,7 +13,9 @@
 //   sp2(z) = log2(1 + 2^z) = softplus(x) / ln 2  for z = x log2 e
 //   pass 1 (LSSAR):    S1_i = sum_j sp2(z_ij),  m_i = max_j z_ij, the softplus sum
 //                      taken as sum_j max(z,0) + log2 prod_j (1 + 2^-|z|)
-//   pass 1 (softmax):  m_i = max_j z_ij
+//   softmax (one pass): a reference maximum per row, raised (and O and the
+//                      row sum rescaled by 2^(old - new)) when a K tile's scores
+//                      exceed it by more than 8; P = 2^(z - ref)
 //   pass 2 weights:    LSSA     w = sp2(z)
 //                      LSSAR    w = max(sp2(z) kappa_i + beta_i, 0)^p with
 //                               theta_i = O_i S1_i / i, kappa_i = 1/(sp2(m_i) - theta_i),
@@ -21,7 +23,7 @@
 //                               ReLU^p(i A - O) divided by its (positive) row maximum,
 //                               which the final L1 normalisation cancels; an all-zero
 //                               row (sp2(m_i) <= theta_i) gets w = 1 (prefix mean)
-//                      softmax  w = 2^(z - m_i)
+//                      softmax  w = 2^(z - ref_i)
 //   ablation modes (the notes' ablation table), both followed by re-weighting:
 //     softmax normaliser  z as in softmax; pass 1: m_i and S1_i = sum_j 2^(z-m_i)
 //                         (running max, sum rescaled per tile); a_ij = 2^(z-m)/S1,
@@ -93,7 +95,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a stuck wait gives up after
 
 // Error codes written to the device error word (first failure wins).
 enum : unsigned { kErrQFull = 1, kErrQEmpty, kErrKvFull, kErrKvEmpty, kErrSFull, kErrSFree,
-                  kErrOFull, kErrOFree, kErrItem, kErrPFull, kErrPFree, kErrDrain, kErrHalves };
+                  kErrOFull, kErrOFree, kErrItem, kErrPFull, kErrPFree, kErrDrain, kErrHalves,
+                  kErrTileMax };
+
+// Softmax (one pass): a row's reference maximum is raised only when a tile's
+// scores exceed it by more than this (log2 units), so P = 2^(z - ref) stays
+// below 2^8 and the rescale of O and of the row sum is rare.
+constexpr float kRescaleLog2 = 8.f;
 
 // Shared-memory descriptor strides.  K-major tiles (Q, K): rows of 128 bytes,
 // 8-row groups 1024 bytes apart.  MN-major V tiles: 16 keys per MMA = 2048
@@ -156,6 +164,7 @@ struct __align__(8) Barriers {
     uint64_t q_full[2], q_empty[2];
     uint64_t s_full[2], s_free[2], o_full[2], o_free[2], p_full[2], p_free[2];
     uint64_t halves[2];   // per Q tile: both column halves have written their row partials
+    uint64_t tile_max[2][4];   // softmax, per Q tile and lane quarter: both halves' tile maxima are in
     uint64_t kv_full[8], kv_empty[8];
     uint64_t item_full[kItemQ], item_empty[kItemQ];
     int item_q[kItemQ];
@@ -494,7 +503,11 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int lane = threadIdx.x & 31;
     constexpr int NS = C::kStages;
     constexpr int TB = C::kTileBytes;
-    constexpr bool kTwoPass = MODE != kLssa;
+    // Plain softmax runs in one pass (online maximum, O rescaled in TMEM);
+    // LSSA needs no statistics pass; the re-weighting modes need the whole
+    // row's first-stage sum before any weight, hence two passes.
+    constexpr bool kOnePassSoftmax = MODE == kSoftmax;
+    constexpr bool kTwoPass = MODE != kLssa && !kOnePassSoftmax;
     constexpr bool kSepP = D == 64;                       // P in TMEM columns of its own
     constexpr bool kExplicitSmem = MODE != kSoftmax;      // exchange arrays by ld/st.shared
     constexpr int kPCol = 2 * kBN;                        // P_w at kPCol + 64 w (d = 64)
@@ -518,6 +531,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::mbar_init(ptx::smem_u32(&bars->p_full[w]), kTileThreads);
             ptx::mbar_init(ptx::smem_u32(&bars->p_free[w]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->halves[w]), kTileThreads);
+            for (int qq = 0; qq < 4; ++qq) ptx::mbar_init(ptx::smem_u32(&bars->tile_max[w][qq]), 64);
         }
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(ptx::smem_u32(&bars->kv_full[s]), 1);
@@ -838,6 +852,15 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t o_free = ptx::smem_u32(&bars->o_free[w]);
         const uint32_t halves = ptx::smem_u32(&bars->halves[w]);   // this tile's two column halves
         uint32_t hv_phase = 0;
+        // softmax: the two warps holding the two column halves of rows
+        // 32 (warp % 4) .. +31 of tile w meet here once per K tile
+        const uint32_t tmax_bar = ptx::smem_u32(&bars->tile_max[w][warp & 3]);
+        uint32_t tm_phase = 0;
+        // this row's two tile-maximum slots (alternating by K tile) and the
+        // offset of the partner half's slot
+        const uint32_t tm_slot0 = ptx::smem_u32(&bars->x_s1[w][h][t]);
+        const uint32_t tm_slot1 = ptx::smem_u32(&bars->x_m[w][h][t]);
+        const uint32_t tm_other = (uint32_t)((h ? -1 : 1) * (int)(kBM * sizeof(float)));
         uint32_t sf_phase = 0, of_phase = 0, qi = 0;
         const float log2e = 1.4426950408889634f;
         auto wait_warp = [&](uint32_t bar, uint32_t parity, unsigned code) -> bool {
@@ -866,7 +889,7 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 rc.a = log2e * prm.ln_d * logf(fi);
             rc.kappa = 0.f;
             rc.beta = 0.f;
-            rc.m = 0.f;
+            rc.m = kOnePassSoftmax ? -INFINITY : 0.f;
             rc.ck = 0.f;
             rc.uniform = false;
             rc.fast = false;
@@ -1008,6 +1031,88 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ptx::tmem_ld_wait();
                 ptx::reg_fence(r0);
                 ptx::reg_fence(r1);
+                if constexpr (kOnePassSoftmax) {
+                    if constexpr (kSepP) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(s_free);   // the next S MMA may start now
+                    }
+                    if (kt == qt) {
+                        to_z<MODE, true>(r0, 64 * h, t, rc.a);
+                        to_z<MODE, true>(r1, 64 * h + 32, t, rc.a);
+                    } else {
+                        to_z<MODE, false>(r0, 64 * h, t, rc.a);
+                        to_z<MODE, false>(r1, 64 * h + 32, t, rc.a);
+                    }
+                    // the row's maximum over this K tile: both column halves'
+                    // maxima meet in shared memory (slots alternate by tile)
+                    float tm = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        tm = max3(tm, __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]));
+                        tm = max3(tm, __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]));
+                    }
+                    const uint32_t slot = (kt & 1) ? tm_slot1 : tm_slot0;
+                    ptx::st_shared_f32(slot, tm);
+                    ptx::mbar_arrive(tmax_bar);
+                    if (!(ok = wait_warp(tmax_bar, tm_phase, kErrTileMax))) break;
+                    tm_phase ^= 1;
+                    tm = fmaxf(tm, ptx::ld_shared_f32(slot + tm_other));
+                    // raise the reference when the tile exceeds it by more than
+                    // kRescaleLog2 (the same decision in both halves: the same
+                    // maxima); O and the row sum are then multiplied by 2^(old - new)
+                    const bool raise = tm > rc.m + kRescaleLog2;
+                    const float alpha = raise ? ptx::ex2(rc.m - tm) : 1.f;
+                    if (raise) {
+                        rc.m = tm;
+                        acc2[0] = __fmul2_rn(acc2[0], make_float2(alpha, alpha));
+                        acc2[1] = __fmul2_rn(acc2[1], make_float2(alpha, alpha));
+                    }
+                    // this tile's weights first (the registers of S are then free)
+                    uint32_t pk0[16], pk1[16];
+                    weights(r0, acc2[0], pk0);
+                    weights(r1, acc2[1], pk1);
+                    // O holds the previous K tiles' P.V once that MMA has
+                    // completed (d = 64: the P-free commit after it; d = 128:
+                    // S(kt), issued after it by the same thread, is complete)
+                    if constexpr (kSepP) {
+                        if (p_pending) {
+                            if (!(ok = wait_warp(p_free, pf_phase, kErrPFree))) break;
+                            pf_phase ^= 1;
+                            ptx::tc_fence_after();
+                            p_pending = false;
+                        }
+                    }
+                    // P first (its registers are free once the stores are issued), then O
+                    ptx::tmem_st16(p_col, pk0);
+                    ptx::tmem_st16(p_col + 16, pk1);
+                    if (__any_sync(0xffffffffu, raise) && kt > 0) {
+                        constexpr int NC = D / 64;   // 32-column chunks of this half's O
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) {
+                            uint32_t oc[32];
+                            ptx::tmem_ld32(o_col + c * 32, oc);
+                            ptx::tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < 32; j += 2) {
+                                const float2 x = __fmul2_rn(
+                                    make_float2(__uint_as_float(oc[j]), __uint_as_float(oc[j + 1])),
+                                    make_float2(alpha, alpha));
+                                oc[j] = __float_as_uint(x.x);
+                                oc[j + 1] = __float_as_uint(x.y);
+                            }
+                            ptx::tmem_st32(o_col + c * 32, oc);
+                        }
+                    }
+                    ptx::tmem_st_wait();
+                    ptx::tc_fence_before();
+                    if constexpr (kSepP) {
+                        ptx::mbar_arrive(p_full);   // P(kt) is in TMEM
+                        p_pending = true;
+                    } else {
+                        ptx::mbar_arrive(s_free);   // P(kt) is in TMEM over the S columns
+                    }
+                    continue;
+                }
                 if constexpr (kSepP) {
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(s_free);   // the next S MMA may start now
