@@ -139,6 +139,25 @@ int lssar_attn_bwd(const void *q, const void *k, const void *v, const void *dout
                    int B, int H, int L, int d, int p, int mode, cudaStream_t stream);
 
 /*
+ * Training with one re-weighting exponent per head (the notes leave an
+ * adaptive or learnable p open: Limitations; training is where such a p would
+ * be chosen).  lssar_attn_fwd_train_heads_p is lssar_attn_fwd_train, and
+ * lssar_attn_bwd_heads_p is lssar_attn_bwd, with head h (of every batch entry)
+ * using p_per_head[h]; pass the same array to both.
+ *   p_per_head : HOST array of H ints, each in 1..1024, read before return.
+ *   mode       : a re-weighting mode (2, 3 or 4); other modes return
+ *                LSSAR_ERR_P.  H must be at most 256 (LSSAR_ERR_P otherwise).
+ * Other arguments, results and errors as lssar_attn_fwd_train / lssar_attn_bwd.
+ */
+int lssar_attn_fwd_train_heads_p(const void *q, const void *k, const void *v, void *out, float *stats,
+                                 int B, int H, int L, int d, const int *p_per_head, int mode,
+                                 cudaStream_t stream);
+int lssar_attn_bwd_heads_p(const void *q, const void *k, const void *v, const void *dout,
+                           const float *stats, void *dq, void *dk, void *dv,
+                           int B, int H, int L, int d, const int *p_per_head, int mode,
+                           cudaStream_t stream);
+
+/*
  * Backward pass: gradients of sum(dout * out) with respect to q, k and v,
  * given the row statistics of the forward (lssar_attn_fwd_train with the same
  * q, k, v, B, H, L, d, p, mode).  Chain rule through the steps of Key designs

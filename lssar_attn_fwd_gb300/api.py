@@ -24,6 +24,8 @@ _EXPORTS = (
     "lssar_attn_fwd_train",
     "lssar_attn_bwd",
     "lssar_attn_bwd_simt",
+    "lssar_attn_fwd_train_heads_p",
+    "lssar_attn_bwd_heads_p",
     "lssar_selftest_stall",
     "lssar_schedule_plan",
     "lssar_decode_plan",
@@ -64,6 +66,12 @@ def load_library():
     lib.lssar_attn_fwd_heads_p.restype = ctypes.c_int
     lib.lssar_attn_fwd_train.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
     lib.lssar_attn_fwd_train.restype = ctypes.c_int
+    lib.lssar_attn_fwd_train_heads_p.argtypes = ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 +
+                                                 [ctypes.POINTER(ctypes.c_int), ctypes.c_int, ctypes.c_void_p])
+    lib.lssar_attn_fwd_train_heads_p.restype = ctypes.c_int
+    lib.lssar_attn_bwd_heads_p.argtypes = ([ctypes.c_void_p] * 8 + [ctypes.c_int] * 4 +
+                                           [ctypes.POINTER(ctypes.c_int), ctypes.c_int, ctypes.c_void_p])
+    lib.lssar_attn_bwd_heads_p.restype = ctypes.c_int
     for name in ("lssar_attn_bwd", "lssar_attn_bwd_simt"):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
@@ -243,6 +251,64 @@ def lssar_attn_fwd_heads_p(q, k, v, p_per_head, mode=MODE_LSSAR, out=None, strea
         _check(call_heads_p(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                             B, H, L, d, p_per_head, mode, s.cuda_stream))
     return out
+
+
+def _int_array(values):
+    arr = (ctypes.c_int * max(1, len(values)))(*[int(x) for x in values])
+    return arr if len(values) else None
+
+
+def call_train_heads_p(q_ptr, k_ptr, v_ptr, out_ptr, stats_ptr, B, H, L, d, p_per_head, mode, stream_handle):
+    """Raw call of lssar_attn_fwd_train_heads_p; returns the status."""
+    return load_library().lssar_attn_fwd_train_heads_p(
+        *(ctypes.c_void_p(x) for x in (q_ptr, k_ptr, v_ptr, out_ptr, stats_ptr)),
+        int(B), int(H), int(L), int(d), _int_array(p_per_head), int(mode), ctypes.c_void_p(stream_handle))
+
+
+def call_bwd_heads_p(ptrs, B, H, L, d, p_per_head, mode, stream_handle):
+    """Raw call of lssar_attn_bwd_heads_p; ptrs as for :func:`call_bwd`."""
+    return load_library().lssar_attn_bwd_heads_p(
+        *(ctypes.c_void_p(x) for x in ptrs), int(B), int(H), int(L), int(d), _int_array(p_per_head),
+        int(mode), ctypes.c_void_p(stream_handle))
+
+
+def lssar_attn_fwd_train_heads_p(q, k, v, p_per_head, mode=MODE_LSSAR, stream=None):
+    """Training forward with one re-weighting exponent per head: returns
+    (out, stats) for :func:`lssar_attn_bwd_heads_p` (same p_per_head)."""
+    import torch
+    if q.device.type != "cuda":
+        raise ValueError("q must be a CUDA tensor")
+    _check_like(q, q, k, v)
+    B, H, L, d = q.shape
+    if len(p_per_head) != H:
+        raise ValueError("p_per_head must hold one exponent per head")
+    out = torch.empty_like(q)
+    stats = torch.empty((B, H, L, 4), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        s = torch.cuda.current_stream(q.device) if stream is None else stream
+        _check(call_train_heads_p(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), stats.data_ptr(),
+                                  B, H, L, d, p_per_head, mode, s.cuda_stream))
+    return out, stats
+
+
+def lssar_attn_bwd_heads_p(q, k, v, dout, stats, p_per_head, mode=MODE_LSSAR, stream=None):
+    """Tensor-core backward with one re-weighting exponent per head, from the
+    statistics of :func:`lssar_attn_fwd_train_heads_p`."""
+    import torch
+    if q.device.type != "cuda":
+        raise ValueError("q must be a CUDA tensor")
+    _check_like(q, q, k, v, dout)
+    B, H, L, d = q.shape
+    if len(p_per_head) != H:
+        raise ValueError("p_per_head must hold one exponent per head")
+    if stats.shape != (B, H, L, 4) or stats.dtype != torch.float32 or not stats.is_contiguous():
+        raise ValueError("stats must be the float32 [B, H, L, 4] tensor of lssar_attn_fwd_train_heads_p")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    with torch.cuda.device(q.device):
+        s = torch.cuda.current_stream(q.device) if stream is None else stream
+        ptrs = tuple(t.data_ptr() for t in (q, k, v, dout, stats, dq, dk, dv))
+        _check(call_bwd_heads_p(ptrs, B, H, L, d, p_per_head, mode, s.cuda_stream))
+    return dq, dk, dv
 
 
 def lssar_attn_decode(q, k_cache, v_cache, p=3, mode=MODE_LSSAR, out=None, stream=None):

@@ -89,6 +89,20 @@ int run_tc(const void *q, const void *k, const void *v, void *out, int B, int H,
     return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
 }
 
+// Checks of a host array of per-head exponents (pure host).
+int check_heads_p(const int *p_per_head, int H, int mode) {
+    if (!p_per_head) return LSSAR_ERR_NULL;
+    if (!lssar::is_reweight(mode)) {
+        if (mode < LSSAR_MODE_SOFTMAX || mode > LSSAR_MODE_SIGMOID_RW) return LSSAR_ERR_MODE;
+        return LSSAR_ERR_P;   // per-head exponents need a re-weighting mode
+    }
+    if (H < 1) return LSSAR_ERR_SHAPE;
+    if (H > kMaxHeadsP) return LSSAR_ERR_P;
+    for (int h = 0; h < H; ++h)
+        if (p_per_head[h] < 1 || p_per_head[h] > kMaxP) return LSSAR_ERR_P;
+    return LSSAR_OK;
+}
+
 // Checks of the backward's arguments (pure host).
 int validate_bwd(const void *q, const void *k, const void *v, const void *dout, const float *stats,
                  void *dq, void *dk, void *dv, int B, int H, int L, int d, int p, int mode,
@@ -166,6 +180,50 @@ int lssar_attn_bwd(const void *q, const void *k, const void *v, const void *dout
     return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
 }
 
+int lssar_attn_fwd_train_heads_p(const void *q, const void *k, const void *v, void *out, float *stats,
+                                 int B, int H, int L, int d, const int *p_per_head, int mode,
+                                 cudaStream_t stream) {
+    const int hst = check_heads_p(p_per_head, H, mode);
+    if (hst != LSSAR_OK) return hst;
+    if (!stats) return LSSAR_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(stats) & 15u) return LSSAR_ERR_ALIGN;
+    lssar::Problem pr;
+    const int st = validate(q, k, v, out, B, H, L, d, p_per_head[0], mode, &pr);
+    if (st != LSSAR_OK) return st;
+    const size_t bytes = (size_t)B * H * L * d * 2, sbytes = (size_t)B * H * L * 16;
+    for (const void *t : {q, k, v, static_cast<const void *>(out)})
+        if (ranges_overlap(stats, sbytes, t, bytes)) return LSSAR_ERR_ALIAS;
+    pr.p_head = p_per_head;
+    pr.stats = stats;
+    cudaMemPool_t pool;
+    if (device_pool(&pool) != cudaSuccess) return LSSAR_ERR_CUDA;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, lssar::tc_workspace_bytes(pr), pool, stream) != cudaSuccess)
+        return LSSAR_ERR_CUDA;
+    const cudaError_t e = lssar::launch_tc(pr, ws, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
+}
+
+int lssar_attn_bwd_heads_p(const void *q, const void *k, const void *v, const void *dout,
+                           const float *stats, void *dq, void *dk, void *dv, int B, int H, int L,
+                           int d, const int *p_per_head, int mode, cudaStream_t stream) {
+    const int hst = check_heads_p(p_per_head, H, mode);
+    if (hst != LSSAR_OK) return hst;
+    lssar::BwdProblem bp;
+    const int st = validate_bwd(q, k, v, dout, stats, dq, dk, dv, B, H, L, d, p_per_head[0], mode, &bp);
+    if (st != LSSAR_OK) return st;
+    bp.p_head = p_per_head;
+    cudaMemPool_t pool;
+    if (device_pool(&pool) != cudaSuccess) return LSSAR_ERR_CUDA;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, lssar::bwd_tc_workspace_bytes(bp), pool, stream) != cudaSuccess)
+        return LSSAR_ERR_CUDA;
+    const cudaError_t e = lssar::launch_bwd_tc(bp, ws, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess) return LSSAR_ERR_CUDA;
+    return e == cudaSuccess ? LSSAR_OK : LSSAR_ERR_CUDA;
+}
+
 int lssar_attn_bwd_simt(const void *q, const void *k, const void *v, const void *dout,
                         const float *stats, void *dq, void *dk, void *dv, int B, int H, int L,
                         int d, int p, int mode, cudaStream_t stream) {
@@ -184,15 +242,8 @@ int lssar_attn_bwd_simt(const void *q, const void *k, const void *v, const void 
 
 int lssar_attn_fwd_heads_p(const void *q, const void *k, const void *v, void *out, int B, int H,
                            int L, int d, const int *p_per_head, int mode, cudaStream_t stream) {
-    if (!p_per_head) return LSSAR_ERR_NULL;
-    if (!lssar::is_reweight(mode)) {
-        if (mode < LSSAR_MODE_SOFTMAX || mode > LSSAR_MODE_SIGMOID_RW) return LSSAR_ERR_MODE;
-        return LSSAR_ERR_P;   // per-head exponents need a re-weighting mode
-    }
-    if (H < 1) return LSSAR_ERR_SHAPE;
-    if (H > kMaxHeadsP) return LSSAR_ERR_P;
-    for (int h = 0; h < H; ++h)
-        if (p_per_head[h] < 1 || p_per_head[h] > kMaxP) return LSSAR_ERR_P;
+    const int hst = check_heads_p(p_per_head, H, mode);
+    if (hst != LSSAR_OK) return hst;
     lssar::Problem pr;
     const int st = validate(q, k, v, out, B, H, L, d, p_per_head[0], mode, &pr);
     if (st != LSSAR_OK) return st;

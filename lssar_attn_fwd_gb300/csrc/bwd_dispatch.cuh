@@ -34,6 +34,7 @@ cudaError_t launch_kernel(const Maps &m, const Params &prm, int grid, cudaStream
 // Re-weighting modes: fixed power chains for p = 3 and 15, square-and-multiply otherwise.
 template <int D, int MODE, int PASS>
 cudaError_t dispatch_p(const BwdProblem &pr, const Maps &m, const Params &prm, int grid, cudaStream_t s) {
+    if (pr.p_head) return launch_kernel<D, MODE, 0, PASS>(m, prm, grid, s);   // per head
     switch (pr.p) {
         case 3: return launch_kernel<D, MODE, 3, PASS>(m, prm, grid, s);
         case 15: return launch_kernel<D, MODE, 15, PASS>(m, prm, grid, s);

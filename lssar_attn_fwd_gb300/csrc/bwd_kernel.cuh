@@ -83,6 +83,9 @@ struct Params {
     int n_items;               // BH * n_tiles
     float ln_d;
     int p;                     // exponent (generic power path)
+    int H;                     // heads per batch entry (for the per-head exponents)
+    int per_head;              // 1: head h uses p_head[h] (generic power path only)
+    int p_head[256];
     const float4 *stats;       // row pass: [BH][L] {m, kappa, beta, W}
     float *rowc;               // [BH][n_tiles][8 fields][128] per-query records (row pass writes)
     unsigned *rmax;            // [BH] max of r_i as float bits (zero before the row pass)
@@ -611,7 +614,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
         uint32_t sf_phase = 0, af_phase = 0, accf_phase = 0, red_phase = 0, qi = 0, ring_idx = 0;
         bool a_pending = false;
         const float log2e = 1.4426950408889634f;
-        const int pe = is_reweight(MODE) ? prm.p : 1;
+        int pe = is_reweight(MODE) ? prm.p : 1;   // this item's exponent (per head when asked)
         auto wait_warp = [&](uint32_t bar, uint32_t parity, unsigned code) -> bool {
             const bool mine = wait_bar(bar, parity, bars, prm.err, code);
             return __all_sync(0xffffffffu, mine);
@@ -654,6 +657,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
             if (!ok || item >= prm.n_items) break;
             int bh, at, p0, p1;
             decode(item, bh, at, p0, p1);
+            if (is_reweight(MODE) && PK == 0 && prm.per_head) pe = prm.p_head[bh % prm.H];
             const int arow = at * kBM + t;                // anchor row (query or key)
             const bool valid = arow < prm.L;
             if (kRow) {

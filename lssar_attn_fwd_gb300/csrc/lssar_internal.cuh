@@ -52,6 +52,7 @@ struct BwdProblem {
     const float *stats;
     void *dq, *dk, *dv;
     int B, H, L, d, p, mode;
+    const int *p_head = nullptr;   // host array of H exponents, or null (one p for all heads)
 };
 // Plain CUDA-core backward; ws holds bwd_simt_workspace_bytes(pr) bytes.
 size_t bwd_simt_workspace_bytes(const BwdProblem &pr);

@@ -177,6 +177,28 @@ def test_backward_invalid_arguments(lib, name):
     assert c(6, DQ + 256) == -8                       # dk overlaps dq
 
 
+def test_train_and_backward_heads_p_invalid_arguments(lib):
+    from lssar_attn_fwd_gb300.api import call_bwd_heads_p, call_train_heads_p
+    good = [3, 15]
+    t = lambda *a: call_train_heads_p(*a, 0)   # noqa: E731
+    assert t(Q, K, V, OUT, STATS, 1, 2, 16, 64, [], 2) == -1            # no array
+    assert t(Q, K, V, OUT, 0, 1, 2, 16, 64, good, 2) == -1              # no stats
+    assert t(Q, K, V, OUT, STATS, 1, 2, 16, 64, good, 0) == -4          # softmax: no p
+    assert t(Q, K, V, OUT, STATS, 1, 2, 16, 64, [3, 0], 2) == -4
+    assert t(Q, K, V, OUT, STATS, 1, 300, 16, 64, [3] * 300, 2) == -4   # > 256 heads
+    assert t(Q, K, V, OUT, STATS + 4, 1, 2, 16, 64, good, 2) == -6
+    assert t(Q, K, V, OUT, Q + 256, 1, 2, 16, 64, good, 2) == -8        # stats inside q
+    assert t(Q, K, V, OUT, STATS, 1, 2, 16, 96, good, 2) == -3
+    ptrs = [Q, K, V, DOUT, STATS, DQ, DK, DV]
+    b = lambda ptrs, H=2, d=64, pp=good, mode=2: call_bwd_heads_p(ptrs, 1, H, 16, d, pp, mode, 0)   # noqa: E731
+    assert b(ptrs, pp=[]) == -1
+    assert b(ptrs, mode=1) == -4
+    assert b(ptrs, pp=[3, 1025]) == -4
+    assert b(ptrs, d=32) == -3
+    assert b(ptrs[:4] + [0] + ptrs[5:]) == -1                          # no stats
+    assert b(ptrs[:5] + [Q + 64] + ptrs[6:]) == -8                     # dq over q
+
+
 @pytest.mark.parametrize("BH,n_qtiles,grid", [(12, 64, 152), (96, 8, 152), (64, 32, 152), (12, 128, 152),
                                               (8, 64, 152), (1, 1, 1), (3, 5, 7), (5, 63, 152), (200, 2, 152)])
 def test_schedule_covers_every_item_once(lib, BH, n_qtiles, grid):

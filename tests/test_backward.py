@@ -291,3 +291,36 @@ def test_backward_tc_uniform_rows(torch_mod):
     ref = reference(qb, kb, vb, db, MODE_LSSAR, 15)
     assert np.abs(to_np(dq)[0, 0, 3:]).max() == 0.0
     assert_close((to_np(dq), to_np(dk), to_np(dv)), ref, MODE_LSSAR, 15)
+
+
+@pytest.mark.parametrize("mode", [MODE_LSSAR, MODE_SIGMOID_RW, MODE_SOFTMAX_RW])
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_tc_per_head_exponents(torch_mod, mode, d):
+    # one exponent per head through the training forward and the backward:
+    # every head's output and gradients against the oracle at its own p
+    from lssar_attn_fwd_gb300 import api
+    torch = torch_mod
+    ps = [1, 3, 15, 7]
+    B, H, L = 2, len(ps), 300
+    qb, kb, vb = make_qkv(B, H, L, d, seed=21 + d + mode)
+    d0 = make_dout(B, H, L, d, seed=21 + d + mode)
+    db = d0.copy()
+    for h, p in enumerate(ps):   # the well-conditioned rows of each head at its own p
+        db[:, h:h + 1] = well_conditioned_dout(qb[:, h:h + 1], kb[:, h:h + 1], d0[:, h:h + 1], mode, p)
+    dropped = int(np.any(db != d0, axis=-1).sum())
+    assert dropped <= max(1, MAX_DROPPED * B * H * L), dropped
+    q, k, v, dout = (to_dev(torch, t) for t in (qb, kb, vb, db))
+    out, stats = api.lssar_attn_fwd_train_heads_p(q, k, v, ps, mode=mode)
+    ref_out = api.lssar_attn_fwd_heads_p(q, k, v, ps, mode=mode)
+    dq, dk, dv = api.lssar_attn_bwd_heads_p(q, k, v, dout, stats, ps, mode=mode)
+    torch.cuda.synchronize()
+    assert api.device_error_word() == 0
+    assert torch.equal(out, ref_out)          # same kernel, same arithmetic as the inference entry
+    got = tuple(to_np(t) for t in (dq, dk, dv))
+    o = to_np(out)
+    for h, p in enumerate(ps):
+        sl = lambda t: t[:, h:h + 1]   # noqa: E731
+        fwd = attention_forward(*(bf16_bits_to_f64(sl(t)) for t in (qb, kb, vb)), mode, p)
+        assert np.abs(sl(o) - fwd).max() <= tol(mode, p), (h, p)
+        ref = reference(*(sl(t) for t in (qb, kb, vb, db)), mode, p)
+        assert_close(tuple(sl(g) for g in got), ref, mode, p, f"head {h} p={p}")
