@@ -41,16 +41,35 @@ class LssarError(RuntimeError):
         self.status = status
 
 
-def lib_path():
-    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "liblssar_attn_fwd.so")
+def lib_path(debug=False):
+    name = "liblssar_attn_fwd_debug.so" if debug else "liblssar_attn_fwd.so"
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", name)
+
+
+_DEBUG_LIB = None
+
+
+def load_debug_library():
+    """Loads the debug-check build of the library (built with
+    ``build(debug=True)``): the same C ABI, with device-side bounds checks
+    that record codes 101-105 in its own device error word.  The functions of
+    this module keep calling the default library; call the debug one through
+    the returned handle (the argument declarations are the same)."""
+    global _DEBUG_LIB
+    if _DEBUG_LIB is None:
+        _DEBUG_LIB = _open(lib_path(debug=True))
+    return _DEBUG_LIB
 
 
 def load_library():
     """Loads the shared library (once).  Raises if it has not been built."""
     global _LIB
-    if _LIB is not None:
-        return _LIB
-    path = lib_path()
+    if _LIB is None:
+        _LIB = _open(lib_path())
+    return _LIB
+
+
+def _open(path):
     if not os.path.exists(path):
         raise RuntimeError(
             f"{path} is missing: build it with `python -m lssar_attn_fwd_gb300.build` "
@@ -90,7 +109,6 @@ def load_library():
     lib.lssar_device_error_word.restype = ctypes.c_int
     lib.lssar_abi_version.argtypes = []
     lib.lssar_abi_version.restype = ctypes.c_int
-    _LIB = lib
     return lib
 
 

@@ -2,7 +2,12 @@
 
 Every ``csrc/*.cu`` is compiled to an object under ``_build/`` (in parallel,
 skipped when up to date) and linked into ``lssar_attn_fwd_gb300/_lib/``.
-Usage: ``python -m lssar_attn_fwd_gb300.build [--force] [--verbose]``.
+``debug=True`` builds liblssar_attn_fwd_debug.so instead (objects under
+``_build_debug/``), compiled with -DLSSAR_DEBUG_CHECKS: the kernels check
+their tensor-copy coordinates, TMEM lane and column ranges, work items and
+global-store indices, and record a code (101-105) in the device error word
+instead of making the access.
+Usage: ``python -m lssar_attn_fwd_gb300.build [--force] [--verbose] [--debug]``.
 """
 
 import concurrent.futures
@@ -16,8 +21,11 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
+DEBUG_BUILD_DIR = os.path.join(ROOT, "_build_debug")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "liblssar_attn_fwd.so"
+DEBUG_LIB_NAME = "liblssar_attn_fwd_debug.so"
+DEBUG_FLAGS = ["-DLSSAR_DEBUG_CHECKS"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -31,13 +39,16 @@ def nvcc_path():
     raise RuntimeError("nvcc not found")
 
 
-def lib_path():
-    return os.path.join(LIB_DIR, LIB_NAME)
+def lib_path(debug=False):
+    return os.path.join(LIB_DIR, DEBUG_LIB_NAME if debug else LIB_NAME)
 
 
 def _flags(extra=()):
     return ARCH + [
-        "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
+        # -fno-gnu-unique: function-local statics of template functions (the
+        # per-device attribute flags of each kernel instance) stay private to
+        # this library instead of being merged with another loaded build's
+        "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fno-gnu-unique",
         "-I", os.path.join(ROOT, "include"), "-I", CSRC,
     ] + list(extra)
 
@@ -47,20 +58,22 @@ def _newest_header():
     return max((os.path.getmtime(h) for h in hs), default=0.0)
 
 
-def build(force=False, verbose=False, ptxas_verbose=False):
-    """Compile and link the library; returns its path."""
+def build(force=False, verbose=False, ptxas_verbose=False, debug=False):
+    """Compile and link the library (the debug-check variant with debug=True);
+    returns its path."""
     nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     if not sources:
         raise RuntimeError("no CUDA sources found")
     hdr_time = _newest_header()
-    extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    extra = (["-Xptxas", "-v"] if ptxas_verbose else []) + (DEBUG_FLAGS if debug else [])
     jobs = []
     objects = []
     for src in sources:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objects.append(obj)
         if (force or not os.path.exists(obj) or os.path.getmtime(obj) < max(os.path.getmtime(src), hdr_time)):
             jobs.append([nvcc] + _flags(extra) + ["-c", src, "-o", obj])
@@ -76,10 +89,14 @@ def build(force=False, verbose=False, ptxas_verbose=False):
                     sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
                 if r.returncode != 0:
                     raise RuntimeError(f"nvcc failed for {cmd[-3]}")
-    out = lib_path()
+    out = lib_path(debug)
     if jobs or not os.path.exists(out):
         tmp = out + ".tmp"
-        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objects
+        # -Bsymbolic and --exclude-libs: the library binds its own functions and
+        # its statically linked CUDA runtime to itself, so that two builds
+        # (default and debug) can be loaded in one process side by side
+        cmd = [nvcc] + ARCH + ["-shared", "-Xlinker", "-Bsymbolic", "-Xlinker", "--exclude-libs,ALL",
+                               "-o", tmp] + objects
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
@@ -90,5 +107,5 @@ def build(force=False, verbose=False, ptxas_verbose=False):
 
 if __name__ == "__main__":
     p = build(force="--force" in sys.argv, verbose="--verbose" in sys.argv,
-              ptxas_verbose="--ptxas" in sys.argv)
+              ptxas_verbose="--ptxas" in sys.argv, debug="--debug" in sys.argv)
     print(p)

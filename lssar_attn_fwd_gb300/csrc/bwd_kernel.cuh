@@ -368,6 +368,9 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 if (item >= prm.n_items) break;
                 int bh, at, p0, p1;
                 decode(item, bh, at, p0, p1);
+                if (!dcheck(bh >= 0 && bh < prm.BH && at >= 0 && at < prm.n_tiles && p0 >= 0 && p1 <= prm.n_tiles,
+                            prm.err, kDbgItem))
+                    break;
                 if (x_cnt > 0 && !wait_all(ptx::smem_u32(&bars->x_empty), (x_cnt - 1) & 1, kErrXEmpty))
                     break;
                 const uint32_t xf = ptx::smem_u32(&bars->x_full);
@@ -391,7 +394,9 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                         }
                         uint8_t *stage = ring + st * C::kStageBytes;
                         const uint32_t full = ptx::smem_u32(&bars->ring_full[st]);
-                        if (ptx::elect_one()) {
+                        // streamed tile and its records inside their tensors
+                        const bool in_range = dcheck(t >= 0 && t < prm.n_tiles, prm.err, kDbgTma);
+                        if (in_range && ptx::elect_one()) {
                             ptx::mbar_arrive_expect_tx(full, 2 * TB + (kRow ? 0 : C::kConstBytes));
 #pragma unroll
                             for (int b = 0; b < D / 64; ++b) {
@@ -609,6 +614,10 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
         const uint32_t a2_col = tmem + lane_addr + (T::kAlias ? T::kDP + 32 * g : T::kA2 + 16 * g);
         const uint32_t acc1_col = tmem + lane_addr + T::kAcc1 + g * (D / 4);
         const uint32_t acc2_col = tmem + lane_addr + T::kAcc2 + g * (D / 4);
+        dcheck(tmem_in_range(s_col, tmem, 32, 512) && tmem_in_range(dp_col, tmem, 32, 512) &&
+                   tmem_in_range(a1_col, tmem, 16, 512) && tmem_in_range(a2_col, tmem, 16, 512) &&
+                   tmem_in_range(acc1_col, tmem, D / 4, 512) && tmem_in_range(acc2_col, tmem, D / 4, 512),
+               prm.err, kDbgTmem);
         const uint32_t s_full = ptx::smem_u32(&bars->s_full), s_free = ptx::smem_u32(&bars->s_free);
         const uint32_t a_full = ptx::smem_u32(&bars->a_full), a_free = ptx::smem_u32(&bars->a_free);
         uint32_t sf_phase = 0, af_phase = 0, accf_phase = 0, red_phase = 0, qi = 0, ring_idx = 0;
@@ -727,8 +736,9 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                     const float dscale = kRaw ? a : 1.f;
                     const float fld[8] = {a, st.x, st.y, st.z, 1.f / st.w, dscale * F, Di, dscale * dS1};
                     float *rec = prm.rowc + ((size_t)bh * prm.n_tiles + at) * 8 * kBN + t;
+                    if (dcheck(bh < prm.BH && at < prm.n_tiles && t < kBN, prm.err, kDbgGlobal))
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) rec[k * kBN] = valid ? fld[k] : 0.f;
+                        for (int k = 0; k < 8; ++k) rec[k * kBN] = valid ? fld[k] : 0.f;
                     if (valid) atomicMax(prm.rmax + bh, __float_as_uint(dscale * (F * dev + fabsf(dS1))));
                 }
                 // pass 2: ds / r into TMEM, dqh accumulates in Acc1
@@ -774,7 +784,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ptx::smem_u32(&bars->acc_free));
-                if (valid) {
+                if (valid && dcheck(bh < prm.BH && arow < prm.L, prm.err, kDbgGlobal)) {
                     float4 *dst = reinterpret_cast<float4 *>(prm.acc_out + ((size_t)bh * prm.L + arow) * D + g * (D / 4));
 #pragma unroll
                     for (int c = 0; c < D / 16; ++c)
@@ -909,7 +919,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 ptx::reg_fence(acc2);
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ptx::smem_u32(&bars->acc_free));
-                if (valid) {
+                if (valid && dcheck(bh < prm.BH && arow < prm.L, prm.err, kDbgGlobal)) {
                     const size_t off = ((size_t)bh * prm.L + arow) * D + g * (D / 4);
                     float4 *dst = reinterpret_cast<float4 *>(prm.acc_out + off);
                     uint4 *dvd = reinterpret_cast<uint4 *>(prm.dv + off);

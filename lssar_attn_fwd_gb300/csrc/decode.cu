@@ -138,7 +138,12 @@ struct Ring {
         const uint32_t bytes = (uint32_t)rows * D * 2;
         const uint32_t full = ptx::smem_u32(&sm->full[s]);
         ptx::mbar_arrive_expect_tx(full, bytes);
-        ptx::bulk_load(ptx::smem_u32(sm->ring[s]), src + (size_t)it * KT * D, bytes, full);
+        // a block of 1..KT whole rows of this chunk, 16-byte aligned at both ends
+        const __nv_bfloat16 *from = src + (size_t)it * KT * D;
+        if (dcheck(rows >= 1 && rows <= KT && (bytes & 15u) == 0 &&
+                       (reinterpret_cast<uintptr_t>(from) & 15u) == 0 && (ptx::smem_u32(sm->ring[s]) & 15u) == 0,
+                   err, kDbgBulk))
+            ptx::bulk_load(ptx::smem_u32(sm->ring[s]), from, bytes, full);
         return true;
     }
     // Issues row blocks [from, to) in order; returns the number issued in total

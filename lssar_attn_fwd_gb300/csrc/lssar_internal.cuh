@@ -14,6 +14,38 @@ __host__ __device__ constexpr bool is_reweight(int mode) { return mode == kLssar
 // Modes whose scores use L2-normalised q, k (prepared by the prologue).
 __host__ __device__ constexpr bool uses_normalised_qk(int mode) { return mode == kLssa || mode == kLssar || mode == kSigmoidRw; }
 
+// Device-side checks of the debug build (compiled with -DLSSAR_DEBUG_CHECKS;
+// in the default build they compile to nothing): a failed check records its
+// code in the device error word and returns false, and the caller skips the
+// access it guards (a skipped copy makes its wait run out, which the bounded
+// waits turn into an error code; nothing traps).
+enum : unsigned {
+    kDbgTma = 101,      // a tensor-copy coordinate outside the tensor or misaligned
+    kDbgTmem = 102,     // a TMEM lane or column range outside the allocation
+    kDbgGlobal = 103,   // a global load or store index outside its tensor
+    kDbgItem = 104,     // a work item outside the schedule
+    kDbgBulk = 105      // a bulk copy outside its source or misaligned
+};
+
+__device__ __forceinline__ bool dcheck(bool ok, unsigned *err, unsigned code) {
+#ifdef LSSAR_DEBUG_CHECKS
+    if (!ok) atomicCAS(err, 0u, code);
+    return ok;
+#else
+    (void)ok;
+    (void)err;
+    (void)code;
+    return true;
+#endif
+}
+
+// TMEM address (lane << 16 | column) of a `width`-column access relative to an
+// allocation of `alloc` columns at `base`: lane below 128, columns inside.
+__device__ __forceinline__ bool tmem_in_range(uint32_t addr, uint32_t base, uint32_t width, uint32_t alloc) {
+    const uint32_t lane = addr >> 16, col = (addr & 0xFFFFu) - (base & 0xFFFFu);
+    return lane < 128u && col + width <= alloc;
+}
+
 // Problem description after validation.  Tensors are [B, H, L, d] bf16.
 struct Problem {
     const void *q;

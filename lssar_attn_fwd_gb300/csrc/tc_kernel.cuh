@@ -595,11 +595,13 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (use > 0 && !wait_all(ptx::smem_u32(&bars->kv_empty[s]), (use - 1) & 1, kErrKvEmpty))
                     return false;
                 const uint32_t full = ptx::smem_u32(&bars->kv_full[s]);
+                const bool in_range = dcheck(tile >= 0 && tile < prm.n_qtiles && bh >= 0 && bh < prm.BH,
+                                             prm.err, kDbgTma);
                 if (ptx::elect_one()) {
                     ptx::mbar_arrive_expect_tx(full, TB);
 #pragma unroll
                     for (int b = 0; b < D / 64; ++b)
-                        ptx::tma_load_3d(ptx::smem_u32(ring + s * TB + b * 16384), map, full, b * 64,
+                        if (in_range) ptx::tma_load_3d(ptx::smem_u32(ring + s * TB + b * 16384), map, full, b * 64,
                                          tile * kBN, bh);
                 }
                 __syncwarp();
@@ -630,6 +632,8 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const int qa = 2 * m, qb = 2 * m + 1;
                 const bool vb = qb < prm.n_qtiles;
                 const int nk = vb ? qb + 1 : qa + 1;
+                if (!dcheck(item >= 0 && m >= 0 && m < prm.n_pairs && bh >= 0 && bh < prm.BH, prm.err, kDbgItem))
+                    break;
                 const uint32_t qbuf = q_cnt % C::kQBufs, quse = q_cnt / C::kQBufs;
                 if (quse > 0 && !wait_all(ptx::smem_u32(&bars->q_empty[qbuf]), (quse - 1) & 1, kErrQEmpty))
                     break;
@@ -720,6 +724,15 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint64_t desc_k0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kKmajorLbo, kKmajorSbo);
         const uint64_t desc_v0 = ptx::smem_desc_sw128(ptx::smem_u32(ring), kVLbo, kVSbo);
         uint32_t qoff = 0;   // byte offset of the current item's Q buffer
+        // the TMEM columns the MMAs write and read stay inside the 512 allocated
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int w = tile(t);
+            dcheck(tmem_in_range(tmem + w * kBN, tmem, kBN, 512) &&
+                       tmem_in_range(tmem + kOCol + w * D, tmem, D, 512) &&
+                       (!kSepP || tmem_in_range(tmem + kPCol + 64 * w, tmem, 64, 512)),
+                   prm.err, kDbgTmem);
+        }
         auto issue_s = [&](int t, uint32_t kslot) {
             const int w = tile(t);
             const uint64_t dq = desc_q0 + (uint64_t)((qoff + w * TB) >> 4);
@@ -845,6 +858,11 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t p_full = ptx::smem_u32(&bars->p_full[w]);
         const uint32_t p_free = ptx::smem_u32(&bars->p_free[w]);
         uint32_t pf_phase = 0;
+        // every TMEM access of this warp stays inside the allocation and in
+        // its own lane quarter
+        dcheck(tmem_in_range(s_col, tmem, 64, 512) && tmem_in_range(o_col, tmem, D / 2, 512) &&
+                   tmem_in_range(p_col, tmem, 32, 512) && ((s_col >> 16) & ~31u) == (uint32_t)((warp & 3) * 32),
+               prm.err, kDbgTmem);
         bool p_pending = false;   // a P.V MMA may still be reading this warpgroup's P words
         const uint32_t s_full = ptx::smem_u32(&bars->s_full[w]);
         const uint32_t s_free = ptx::smem_u32(&bars->s_free[w]);
@@ -1194,9 +1212,10 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                     st.z = 0.f;
                     st.w = s2;
                 }
-                prm.stats[(size_t)bh * prm.L + row] = st;
+                if (dcheck(bh < prm.BH && row < prm.L, prm.err, kDbgGlobal))
+                    prm.stats[(size_t)bh * prm.L + row] = st;
             }
-            if (row < prm.L) {
+            if (row < prm.L && dcheck(bh >= 0 && bh < prm.BH, prm.err, kDbgGlobal)) {
                 const float inv = 1.f / s2;
                 uint4 *dst = reinterpret_cast<uint4 *>(prm.out + ((size_t)bh * prm.L + row) * D +
                                                        h * (D / 2));
