@@ -14,6 +14,7 @@ namespace lssar {
 // for this code by minimax (Lawson-weighted least squares) on [0, 1] with the
 // constant term fixed at 0, so that a masked column (z = -inf: u = 0) still
 // gives exactly 0; the largest error is 2.2e-6 in fp32 Horner arithmetic.
+// fit_softplus_poly.py beside this file reproduces them (and fits other degrees).
 __device__ __forceinline__ float2 sp2x2_poly(float2 z) {
     const float2 u = make_float2(ptx::ex2(-fabsf(z.x)), ptx::ex2(-fabsf(z.y)));
     float2 h = __ffma2_rn(u, make_float2(-0.02645743452012539f, -0.02645743452012539f),

@@ -63,3 +63,16 @@ def test_polynomial_is_monotone():
     # rose and fell could reorder nearby scores
     u = np.linspace(0.0, 1.0, 100_001)
     assert np.all(np.diff(poly_f32(u).astype(np.float64)) >= -1e-7)
+
+
+def test_coefficients_are_reproduced_by_the_fitting_script():
+    # the committed fit (Lawson minimax, constant term 0), rounded to fp32,
+    # gives exactly the header's coefficients
+    import importlib.util
+    path = HEADER.parent / "fit_softplus_poly.py"
+    spec = importlib.util.spec_from_file_location("fit_softplus_poly", path)
+    fit = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(fit)
+    c = fit.fit(6)
+    assert [np.float32(x) for x in c] == [np.float32(x) for x in coefficients()]
+    assert fit.max_error_f32(c) < 2.3e-6
