@@ -19,6 +19,14 @@ cudaError_t launch_kernel(const CUtensorMap &mq, const CUtensorMap &mk, const CU
     constexpr int smem = Cfg<D>::kSmemBytes;
     static PerDeviceOnce once;
     cudaError_t e = per_device_once(once, nullptr, [&](int &) {
+        // the kernel moves registers from its control warpgroup to its score
+        // warpgroups (setmaxnreg): that split adds up only for a launch at
+        // exactly kLaunchRegs registers per thread, so any other allocation
+        // is refused here rather than launched
+        cudaFuncAttributes attr;
+        cudaError_t a = cudaFuncGetAttributes(&attr, kern);
+        if (a != cudaSuccess) return a;
+        if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (e != cudaSuccess) return e;

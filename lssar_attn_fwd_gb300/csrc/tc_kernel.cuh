@@ -35,16 +35,19 @@
 //                         for this mode (scale -a, mask +inf) so 2^-z needs no negation.
 //   out_i = (sum_j w_ij v_j) / (sum_j w_ij)
 //
-// Structure (one persistent CTA per SM; 608 threads = 19 warps at d = 64, 576 at d = 128):
+// Structure (one persistent CTA per SM; 640 threads = 20 warps at d = 64, 576
+// = 18 warps at d = 128):
 //   warp 0      TMA producer: Q tiles once per work item, then K (pass 1) and
 //               K, V (pass 2) tiles through an NS-stage shared-memory ring.
 //   warp 1      TMEM owner and tcgen05.mma issuer: for Q tile 0 of the pair at
 //               d = 64, for both tiles at d = 128.
-//   warp 18     (d = 64) tcgen05.mma issuer for Q tile 1.  Each issuer runs its
+//   warp 2      (d = 64) tcgen05.mma issuer for Q tile 1.  Each issuer runs its
 //               tile's chain of waits, MMAs and commits on its own, so the two
 //               chains overlap; both walk the whole K/V ring and each releases
-//               every stage.
-//   warps 2-17  four score warpgroups g = 0..3: Q tile w = g & 1 of the pair,
+//               every stage.  Warp 3 (d = 64) has no role: warps 0-3 form the
+//               control warpgroup, which hands registers to the score warps.
+//   score warps four warpgroups g = 0..3 (warps 4-19 at d = 64, 2-17 at
+//               d = 128): Q tile w = g & 1 of the pair,
 //               column half h = g >> 1 of its 128-key S tile.  Thread t of a
 //               warpgroup owns query row t (TMEM lane t, lane quarter = warp % 4)
 //               and keys [64h, 64h+64) of every tile: it reads S from TMEM,
@@ -54,8 +57,10 @@
 //               a row combine their partial sums and maxima once per item
 //               through shared memory (a per-tile mbarrier, bounded wait).
 // The control warps run their loops warp-wide (one elected lane issues each
-// copy, MMA and commit).  Eighteen or nineteen warps put five on some SM
-// sub-partitions, which caps the registers at 96 per thread.
+// copy, MMA and commit).  Eighteen or twenty warps put five on some SM
+// sub-partitions, which caps the launch at 96 registers per thread; at d = 64
+// the control warpgroup then drops to 64 and the score warpgroups rise to 104
+// (setmaxnreg; the host launches only at exactly 96).
 // d = 64: P has TMEM columns of its own, so a warpgroup releases S as soon as
 // it has loaded it and the next S MMA overlaps the weight computation; P is
 // double-checked free by a commit after each P.V MMA.  d = 128: TMEM is full
@@ -89,8 +94,16 @@ namespace tc {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kScoreWarp0 = 2;    // first score warp (warps 2-17)
-constexpr int kMmaWarp1 = 18;     // second MMA issuer, when there are two
+constexpr int kMmaWarp1 = 2;      // second MMA issuer (d = 64)
+// Registers per thread.  Every instance is launched with kLaunchRegs; at
+// d = 64 the control warpgroup (warps 0-3) then gives registers back and the
+// four score warpgroups take them: 128 x 64 + 512 x 104 = 640 x 96.  (At
+// d = 128 the one MMA warp, which orders both tiles' MMAs, needs more than 64
+// registers: that layout keeps 96 everywhere.)
+constexpr int kLaunchRegs = 96;
+constexpr int kCtrlRegs = 64;
+constexpr int kScoreRegs = 104;
+static_assert(128 * kCtrlRegs + 512 * kScoreRegs <= 640 * kLaunchRegs, "register split");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a stuck wait gives up after 2 s
 
 // Error codes written to the device error word (first failure wins).
@@ -152,7 +165,12 @@ struct Cfg {
     // MMA-issuing warps: one per Q tile at d = 64 (P in columns of its own);
     // at d = 128, where P is written over S, one warp orders both tiles' MMAs.
     static constexpr int kMmaWarps = D == 64 ? 2 : 1;
-    static constexpr int kThreads = 576 + 32 * (kMmaWarps - 1);
+    // d = 64: a control warpgroup (warps 0-3: producer, two MMA issuers, one
+    // idle) and score warps 4-19 with the register split; d = 128: producer
+    // and MMA warp 0-1, score warps 2-17, no split
+    static constexpr bool kSplit = D == 64;
+    static constexpr int kScoreWarp0 = kSplit ? 4 : 2;
+    static constexpr int kThreads = 32 * kScoreWarp0 + 512;
 };
 
 constexpr int kItemQ = 4;                     // depth of the work-item queue
@@ -579,6 +597,8 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         return __all_sync(0xffffffffu, wait_bar(bar, parity, bars, prm.err, code, honour_abort));
     };
 
+    if (warp < C::kScoreWarp0) {
+    if constexpr (C::kSplit) ptx::setmaxnreg_dec<kCtrlRegs>();   // the control warpgroup gives registers back
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         // (the whole warp runs the loop; one elected lane issues the copies)
@@ -845,9 +865,11 @@ lssar_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             commit(&bars->q_empty[qbuf]);
         }
         __syncwarp();
+    }   // warp 3 of the control warpgroup (d = 64) has no role
     } else {
+        if constexpr (C::kSplit) ptx::setmaxnreg_inc<kScoreRegs>();   // each score warpgroup takes them
         // ------------------------------------------------------------ score warpgroups
-        const int g = (warp - kScoreWarp0) >> 2;    // 0..3
+        const int g = (warp - C::kScoreWarp0) >> 2;    // 0..3
         const int w = g & 1;                        // Q tile of the pair
         const int h = g >> 1;                       // column half of the S tile
         const int t = (warp & 3) * 32 + lane;       // row within the Q tile = TMEM lane
