@@ -74,7 +74,8 @@ def kernel_source_sha():
     counters still apply."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("tc_kernel.cuh", "softplus_poly.cuh", "tc_ptx.cuh", "lssar_internal.cuh", "tc_dispatch.cuh"):
+    for name in ("tc_kernel.cuh", "fast_weights.cuh", "softplus_poly.cuh", "tc_ptx.cuh", "lssar_internal.cuh",
+                 "tc_dispatch.cuh"):
         with open(os.path.join(ROOT, "lssar_attn_fwd_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -50,6 +50,7 @@
 
 #include <type_traits>
 
+#include "fast_weights.cuh"
 #include "lssar_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -58,6 +59,8 @@ namespace tcb {
 
 using Diag = std::true_type;       // the causal diagonal tile of an item
 using OffDiag = std::false_type;   // a tile without masked elements
+using Fast = std::true_type;       // one-exponential LSSAR weights (rows within the bound)
+using Exact = std::false_type;     // log2(1 + 2^z) weights
 
 constexpr int kBM = 128;                  // anchor rows of an item (TMEM lanes)
 constexpr int kBN = 128;                  // partner rows of a streamed tile
@@ -85,6 +88,7 @@ struct Params {
     int p;                     // exponent (generic power path)
     int H;                     // heads per batch entry (for the per-head exponents)
     int per_head;              // 1: head h uses p_head[h] (generic power path only)
+    int exact_weights;         // 1: LSSAR rows never take the one-exponential weights
     int p_head[256];
     const float4 *stats;       // row pass: [BH][L] {m, kappa, beta, W}
     float *rowc;               // [BH][n_tiles][8 fields][128] per-query records (row pass writes)
@@ -240,6 +244,28 @@ __device__ __forceinline__ Elem element(float2 z, float2 m, float2 kappa, float2
     return r;
 }
 
+// LSSAR on a row whose one-exponential bound holds (for p and p - 1): the
+// weight's softplus as z + e / ln 2 with e = 2^-|z| (the forward's weight
+// pass does the same on such rows), and the exact logistic slope from the
+// same exponential, phi'(z) = 1 / (1 + e) for z >= 0 and e / (1 + e) below.
+// With Slope false the slope is left out (the statistics sweep needs none).
+template <int PK, bool Slope>
+__device__ __forceinline__ Elem element_fast(float2 z, float2 kappa, float2 beta, float2 ck, int p) {
+    Elem r;
+    const float2 e = make_float2(ptx::ex2(-fabsf(z.x)), ptx::ex2(-fabsf(z.y)));
+    const float2 base = ptx::fma_sat2(e, ck, __ffma2_rn(z, kappa, beta));
+    r.u = pow_pm1<PK>(base, p);
+    r.w = __fmul2_rn(r.u, base);
+    if constexpr (Slope) {
+        const float2 e1 = __fadd2_rn(e, make_float2(1.f, 1.f));
+        const float2 rc = make_float2(ptx::rcp(e1.x), ptx::rcp(e1.y));
+        r.slope = __fmul2_rn(rc, make_float2(z.x >= 0.f ? 1.f : e.x, z.y >= 0.f ? 1.f : e.y));
+    } else {
+        r.slope = make_float2(0.f, 0.f);
+    }
+    return r;
+}
+
 template <int MODE>
 __device__ __forceinline__ uint32_t pack_ds(float lo, float hi) {
     if constexpr (uses_normalised_qk(MODE))
@@ -259,6 +285,9 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
     constexpr int TB = C::kTB;
     constexpr bool kRaw = !uses_normalised_qk(MODE);
     constexpr bool kRow = PASS == kRowPass;
+    // the row pass's LSSAR sweeps have a one-exponential variant (p = 15 and
+    // the generic power path; at p = 3 the bound never holds)
+    constexpr bool kFastModes = kRow && MODE == kLssar && (PK == 15 || PK == 0);
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base as an offset from the array itself: a pointer
     // rebuilt from an integer would lose the shared address space, and every
@@ -677,14 +706,27 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 const float a = !valid ? 0.f : (kRaw ? log2e * rsqrtf((float)D) : log2e * prm.ln_d * logf(fi));
                 const float F = (float)pe * st.y / st.w;
                 const float2 mm = make_float2(st.x, st.x), kk = make_float2(st.y, st.y), bb = make_float2(st.z, st.z);
+                // LSSAR rows whose one-exponential bound holds for p and p - 1
+                // (threshold theta = -beta / kappa) take the forward's
+                // one-exponential weights; the choice is warp-uniform
+                bool fastw = false;
+                float2 ck = make_float2(0.f, 0.f);
+                if constexpr (kFastModes) {
+                    const bool mine = !valid || (st.y > 0.f && fast_weights_ok(-st.z / st.y, st.y, fi, pe) &&
+                                                 fast_weights_ok(-st.z / st.y, st.y, fi, pe - 1));
+                    fastw = !prm.exact_weights && __all_sync(0xffffffffu, mine);
+                    ck = make_float2(2.f * kHalfInvLn2 * st.y, 2.f * kHalfInvLn2 * st.y);
+                }
                 float2 e_acc = make_float2(0.f, 0.f), du_acc = make_float2(0.f, 0.f), u_acc = make_float2(0.f, 0.f);
                 float dmax = -INFINITY, dmin = INFINITY;
-                auto stats_tile = [&](const uint32_t (&rs)[32], const uint32_t (&rd)[32], auto diag) {
+                auto stats_tile = [&](const uint32_t (&rs)[32], const uint32_t (&rd)[32], auto diag, auto fast) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
                         const float2 z = score_z<MODE>(rs[c], rs[c + 1], a);
                         float2 dP = make_float2(__uint_as_float(rd[c]), __uint_as_float(rd[c + 1]));
-                        Elem el = element<MODE, PK>(z, mm, kk, bb, pe);
+                        Elem el;
+                        if constexpr (decltype(fast)::value) el = element_fast<PK, false>(z, kk, bb, ck, pe);
+                        else el = element<MODE, PK>(z, mm, kk, bb, pe);
                         float2 lo = dP, hi = dP;
                         if constexpr (decltype(diag)::value) {
                             if (32 * g + c > t) { el.w.x = 0.f; el.u.x = 0.f; lo.x = INFINITY; hi.x = -INFINITY; }
@@ -700,8 +742,9 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 for (int kt = p0; kt < p1; ++kt) {
                     uint32_t rs[32], rd[32];
                     if (!(ok = load_scores(rs, rd))) break;
-                    if (kt == at) stats_tile(rs, rd, Diag());
-                    else stats_tile(rs, rd, OffDiag());
+                    if (kt == at) stats_tile(rs, rd, Diag(), Exact());
+                    else if (kFastModes && fastw) stats_tile(rs, rd, OffDiag(), Fast());
+                    else stats_tile(rs, rd, OffDiag(), Exact());
                 }
                 if (!ok) break;
                 bars->x_red[0][g][t] = e_acc.x + e_acc.y;
@@ -743,12 +786,14 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 }
                 // pass 2: ds / r into TMEM, dqh accumulates in Acc1
                 auto ds_tile = [&](const uint32_t (&rs)[32], const uint32_t (&rd)[32], uint32_t (&w1)[16],
-                                   auto diag) {
+                                   auto diag, auto fast) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
                         const float2 z = score_z<MODE>(rs[c], rs[c + 1], a);
                         const float2 dP = make_float2(__uint_as_float(rd[c]), __uint_as_float(rd[c + 1]));
-                        const Elem el = element<MODE, PK>(z, mm, kk, bb, pe);
+                        Elem el;
+                        if constexpr (decltype(fast)::value) el = element_fast<PK, true>(z, kk, bb, ck, pe);
+                        else el = element<MODE, PK>(z, mm, kk, bb, pe);
                         const float2 dd = __fadd2_rn(dP, make_float2(-Di, -Di));
                         const float2 gg = __ffma2_rn(__fmul2_rn(dd, el.u), make_float2(Fp, Fp), make_float2(dS1p, dS1p));
                         float2 ds = __fmul2_rn(gg, el.slope);
@@ -763,8 +808,9 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                     uint32_t rs[32], rd[32];
                     if (!(ok = load_scores(rs, rd))) break;
                     uint32_t w1[16];
-                    if (kt == at) ds_tile(rs, rd, w1, Diag());
-                    else ds_tile(rs, rd, w1, OffDiag());
+                    if (kt == at) ds_tile(rs, rd, w1, Diag(), Exact());
+                    else if (kFastModes && fastw) ds_tile(rs, rd, w1, OffDiag(), Fast());
+                    else ds_tile(rs, rd, w1, OffDiag(), Exact());
                     if (!(ok = store_a(w1, w1))) break;
                 }
                 if (!ok) break;

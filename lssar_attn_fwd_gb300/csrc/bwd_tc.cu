@@ -147,6 +147,7 @@ cudaError_t launch_bwd_tc(const BwdProblem &pr, void *ws, cudaStream_t stream) {
     prm.p = pr.p;
     prm.H = pr.H;
     prm.per_head = pr.p_head ? 1 : 0;
+    prm.exact_weights = exact_weights_requested() ? 1 : 0;
     for (int h = 0; h < 256; ++h) prm.p_head[h] = (pr.p_head && h < pr.H) ? pr.p_head[h] : pr.p;
     prm.stats = reinterpret_cast<const float4 *>(pr.stats);
     prm.rowc = reinterpret_cast<float *>(base + lay.rowc);

@@ -299,8 +299,7 @@ cudaError_t launch_tc(const Problem &pr, void *ws, cudaStream_t stream, const Ev
     prm.per_head = pr.p_head ? 1 : 0;
     // LSSAR_EXACT_WEIGHTS=1 keeps every row on the two-transcendental softplus
     // in pass 2 (a cross-check of the one-exponential weights)
-    const char *exact = getenv("LSSAR_EXACT_WEIGHTS");
-    prm.exact_weights = (exact != nullptr && exact[0] == '1') ? 1 : 0;
+    prm.exact_weights = exact_weights_requested() ? 1 : 0;
     for (int h = 0; h < tc::kMaxHeadsP; ++h) prm.p_head[h] = (pr.p_head && h < pr.H) ? pr.p_head[h] : pr.p;
     prm.out = static_cast<__nv_bfloat16 *>(pr.out);
     prm.stats = reinterpret_cast<float4 *>(pr.stats);
@@ -331,6 +330,11 @@ int schedule_plan(int BH, int n_qtiles, int grid, int *first, int *tail_base) {
     for (int i = 0; i < 2 * grid; ++i) first[i] = sch.first[i];
     *tail_base = sch.tail_base;
     return 0;
+}
+
+bool exact_weights_requested() {
+    const char *exact = getenv("LSSAR_EXACT_WEIGHTS");
+    return exact != nullptr && exact[0] == '1';
 }
 
 cudaError_t read_and_clear_error_word(unsigned int *word) {

@@ -324,3 +324,58 @@ def test_backward_tc_per_head_exponents(torch_mod, mode, d):
         assert np.abs(sl(o) - fwd).max() <= tol(mode, p), (h, p)
         ref = reference(*(sl(t) for t in (qb, kb, vb, db)), mode, p)
         assert_close(tuple(sl(g) for g in got), ref, mode, p, f"head {h} p={p}")
+
+
+@pytest.mark.parametrize("p", [15, 40])
+def test_backward_tc_one_exponential_weights(torch_mod, p, monkeypatch):
+    # The row pass takes the forward's one-exponential weights (softplus as
+    # z + 2^-|z| / ln 2) on warps (32 query rows) whose rows all meet the error
+    # bound at p and at p - 1; LSSAR_EXACT_WEIGHTS=1 keeps log2(1 + 2^z)
+    # everywhere.  With the same row statistics the two backward results are
+    # bit-identical on every warp that the bound rejects, differ somewhere on
+    # the admitted warps (a change of about 1e-6 of a weight flips the bf16
+    # rounding of few dq elements), and both match the oracle's gradients
+    # element by element.  The bound is recomputed here in float64 from the
+    # saved statistics (theta = -beta / kappa), with a margin of 2x either
+    # way around the kernel's float32 decision.  p = 40: generic power path.
+    from test_fast_weights import FAST_BOUND, admitted
+    from lssar_attn_fwd_gb300 import api
+    torch = torch_mod
+    B, H, L, d = 1, 2, 2048, 64
+    qb, kb, vb = make_qkv(B, H, L, d, seed=31 + p)
+    d0 = make_dout(B, H, L, d, seed=31 + p)
+    db = well_conditioned_dout(qb, kb, d0, MODE_LSSAR, p)
+    dropped = int(np.any(db != d0, axis=-1).sum())
+    assert dropped <= max(1, MAX_DROPPED * B * H * L), dropped
+    q, k, v, dout = (to_dev(torch, t) for t in (qb, kb, vb, db))
+    monkeypatch.delenv("LSSAR_EXACT_WEIGHTS", raising=False)
+    _, stats = api.lssar_attn_fwd_train(q, k, v, p=p, mode=MODE_LSSAR)
+    fast = api.lssar_attn_bwd(q, k, v, dout, stats, p=p, mode=MODE_LSSAR)
+    monkeypatch.setenv("LSSAR_EXACT_WEIGHTS", "1")
+    exact = api.lssar_attn_bwd(q, k, v, dout, stats, p=p, mode=MODE_LSSAR)
+    monkeypatch.delenv("LSSAR_EXACT_WEIGHTS")
+    torch.cuda.synchronize()
+    assert api.device_error_word() == 0
+    got_f, got_e = tuple(to_np(t) for t in fast), tuple(to_np(t) for t in exact)
+    st = stats.cpu().numpy().astype(np.float64)
+    kap, bet = st[..., 1], st[..., 2]
+    live = kap > 0
+    theta = np.where(live, -bet / np.where(live, kap, 1.0), 0.0)
+    i = np.arange(1, L + 1, dtype=np.float64)
+    _, b_p = admitted(theta, np.where(live, kap, 1.0), i, p)
+    _, b_q = admitted(theta, np.where(live, kap, 1.0), i, p - 1)
+    bound = np.maximum(b_p, b_q)
+    sure_out = ~live | (theta < 1.49) | (bound > 2.0 * FAST_BOUND)
+    sure_in = live & (theta > 1.51) & (bound < 0.5 * FAST_BOUND)
+    warp_out = np.repeat(sure_out.reshape(B, H, L // 32, 32).any(-1), 32, axis=-1)
+    warp_in = np.repeat(sure_in.reshape(B, H, L // 32, 32).all(-1), 32, axis=-1)
+    warp_in[..., :128] = False     # the first tile has only its diagonal tile: exact weights
+    moved = np.any(got_f[0] != got_e[0], axis=-1)
+    print(f"p {p}: warps admitted {warp_in.mean():.3f}, rejected {warp_out.mean():.3f}; "
+          f"dq rows moved {moved.mean():.4f} (admitted warps: {moved[warp_in].mean():.4f})")
+    assert warp_in.mean() > 0.3 and warp_out.mean() > 0.05
+    assert not moved[warp_out].any()
+    assert moved[warp_in].any()
+    ref = reference(qb, kb, vb, db, MODE_LSSAR, p)
+    assert_close(got_f, ref, MODE_LSSAR, p, "one-exponential")
+    assert_close(got_e, ref, MODE_LSSAR, p, "exact")

@@ -110,3 +110,23 @@ def test_wrong_constant_breaks_the_bound():
     for ok, bound, rel, dout, vmax in run_case("iid", 2048, 64, 15, c1=1.0):
         broken |= bool((rel[ok] > bound[ok]).any())
     assert broken
+
+
+@pytest.mark.parametrize("p", [15, 40])
+def test_backward_factor_stays_within_the_bound_at_p_minus_1(p):
+    # The backward's row pass needs u = y^(p-1) as well as w = y^p: on rows
+    # admitted at both p and p - 1, the sum of u over the row moves by at
+    # most the bound at p - 1, relative to that sum (the same argument with
+    # p - 1 in place of p; the row maximum has u = 1, so the sum is >= 1).
+    qb, kb, vb = make_qkv(1, 2, 2048, 64, seed=12)
+    qf, kf = (bf16_bits_to_f64(t)[0] for t in (qb, kb))
+    for h in range(2):
+        z, mask, i = row_terms(qf[h], kf[h], 64)
+        _, _, theta, kappa = weights(z, mask, i, p)
+        ok_p, _ = admitted(theta, kappa, i, p)
+        ok_q, bound_q = admitted(theta, kappa, i, p - 1)
+        ok = ok_p & ok_q
+        u, uf, _, _ = weights(z, mask, i, p - 1)
+        rel = np.abs(uf - u).sum(1) / u.sum(1)
+        assert ok.mean() > 0.5, ok.mean()
+        assert (rel[ok] <= bound_q[ok]).all()
