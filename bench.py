@@ -462,6 +462,10 @@ def run_ours(args, wl, mode, p):
                                 "overlap the kernel of step i (two device buffer sets)",
                     "serial": {"value": whole_job_tflops(ws, F, serial_ms), "ms_per_step": serial_ms,
                                "note": "copies and kernel back to back on one stream"},
+                    "l2": "no flush between steps: every step's inputs are written by that step's "
+                          "host-to-device copy, and the kernel reads them where the copy left them "
+                          "(in L2 when they fit, as in a user's input pipeline); the device-resident "
+                          "value flushes L2 before every step instead",
                     "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2},
             "gpu_launches": K * launches_per_step,
             "clocks": sampler.summary(load0, load1, timed=(w0, w1)) if sampler else None,
