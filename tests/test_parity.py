@@ -279,8 +279,9 @@ def bf16_ulp(x):
     return 2.0 ** (np.floor(np.log2(ax)) - 7)
 
 
-@pytest.mark.parametrize("structure,p,min_moved", [("iid", 15, 0.5), ("needle", 15, 0.0), ("iid", 64, 0.2)])
-def test_one_exponential_weights(torch_mod, structure, p, min_moved, monkeypatch):
+@pytest.mark.parametrize("structure,p,min_moved,d", [("iid", 15, 0.5, 64), ("needle", 15, 0.0, 64),
+                                                     ("iid", 64, 0.2, 64), ("iid", 15, 0.5, 128)])
+def test_one_exponential_weights(torch_mod, structure, p, min_moved, d, monkeypatch):
     # LSSAR rows whose error bound holds take z + 2^-|z|/ln 2 for the softplus
     # in the weight pass; LSSAR_EXACT_WEIGHTS=1 keeps log2(1 + 2^z) on every row.
     # The row sums W = sum_j w_j saved by the training forward show which rows
@@ -289,7 +290,7 @@ def test_one_exponential_weights(torch_mod, structure, p, min_moved, monkeypatch
     # rounding step, and both match the oracle on sampled rows.
     from lssar_attn_fwd_gb300 import api
     torch = torch_mod
-    B, H, L, d = 1, 2, 8192, 64
+    B, H, L = 1, 2, 8192
     qb, kb, vb = make_qkv(B, H, L, d, seed=5, structure=structure)
     q, k, v = (to_dev(torch, t) for t in (qb, kb, vb))
     monkeypatch.delenv("LSSAR_EXACT_WEIGHTS", raising=False)
