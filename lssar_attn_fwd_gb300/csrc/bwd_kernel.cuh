@@ -19,12 +19,14 @@
 //     pass 1 over the key tiles: S = Qh Kh^T, dP = dO V^T; per row D_i, the
 //     sum for dS1_i and the range of dP (which bounds |ds| for the fp16 scale
 //     r_i); pass 2: S, dP again, ds / r_i -> TMEM, dQh += (ds / r_i) Kh.
-//     Writes dqh (fp32), the per-query record used by the column pass, and the
+//     Writes dq (the gradient of the row normalisation applied to dqh in the
+//     epilogue), the per-query record used by the column pass, and the
 //     per-head maximum R of r_i.
 //   column pass (PASS = kColPass), one item per 128-key tile, anchor = (kh, v):
 //     one pass over the query tiles i >= j: S^T = Kh Qh^T, dP^T = V dO^T,
 //     P^T and ds^T / R -> TMEM, dV += P^T dO, dKh += (ds^T / R) Qh.  The
-//     query records arrive with each tile (bulk copy into the stage).
+//     query records arrive with each tile (bulk copy into the stage).  Writes
+//     dv and dk (the normalisation gradient applied to dkh in the epilogue).
 // In the normalised modes the prologue writes the query rows as a_i qh_i
 // (fp16), exactly as the forward does, so S is z itself; the column pass's
 // product with those rows then takes ds_ij / a_i.
@@ -75,7 +77,7 @@ enum Pass : int { kRowPass = 0, kColPass = 1 };
 
 // Error codes in the device error word (the forward kernel uses 1-11).
 enum : unsigned { kErrXFull = 21, kErrXEmpty, kErrRingFull, kErrRingEmpty, kErrSFull, kErrSFree,
-                  kErrAFull, kErrAFree, kErrAccFull, kErrAccFree, kErrItem, kErrRed, kErrDrain };
+                  kErrAFull, kErrAFree, kErrAccFull, kErrAccFree, kErrItem, kErrRed, kErrDrain, kErrFin };
 
 constexpr uint32_t kKmajorLbo = 16, kKmajorSbo = 1024;    // K-major tiles
 constexpr uint32_t kMnLbo = 16384, kMnSbo = 1024;         // the same tiles read MN-major
@@ -93,7 +95,8 @@ struct Params {
     const float4 *stats;       // row pass: [BH][L] {m, kappa, beta, W}
     float *rowc;               // [BH][n_tiles][8 fields][128] per-query records (row pass writes)
     unsigned *rmax;            // [BH] max of r_i as float bits (zero before the row pass)
-    float *acc_out;            // row pass: dqh, column pass: dkh; [BH][L][D] fp32
+    const __nv_bfloat16 *xraw; // row pass: q, column pass: k (raw rows, for the normalisation gradient)
+    __nv_bfloat16 *grad;       // row pass: dq, column pass: dk; [BH][L][D]
     __nv_bfloat16 *dv;         // column pass: dv [BH][L][D]
     unsigned *err;             // device error word
     unsigned *counter;         // work counter, zero at launch
@@ -107,7 +110,7 @@ struct Cfg {
     static constexpr int kStages = D == 64 ? 4 : 2;
     static constexpr int kRingOff = 2 * kTB;                   // after the two anchor tiles
     static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-    static constexpr int kBarBytes = 12288;
+    static constexpr int kBarBytes = 16384;
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
 };
 
@@ -125,19 +128,22 @@ struct Tmem {
     static constexpr uint32_t kItemConsumers = kIssuers + kMathThreads;
 };
 static_assert(Tmem<128, kRowPass>::kA1 + 64 <= 512 && Tmem<64, kColPass>::kA2 + 64 <= 512, "TMEM");
+static_assert(Cfg<64>::kSmemBytes <= 232448 && Cfg<128>::kSmemBytes <= 232448, "shared memory per CTA");
 
 struct __align__(8) Barriers {
     uint64_t x_full, x_empty;
     uint64_t ring_full[4], ring_empty[4];
     uint64_t s_full, s_free, a_full, a_free, acc_full, acc_free;
     uint64_t red;              // row pass: the four warpgroups' partials are in x_red
+    uint64_t fin;              // epilogue: the four warpgroups' partials are in x_fin
     uint64_t item_full[kItemQ], item_empty[kItemQ];
     int item_q[kItemQ];
     uint32_t tmem_base;
     int abort_flag;
     float x_red[5][4][kBM];    // row pass: partial row sums of the four warpgroups
+    float x_fin[2][4][kBM];    // epilogue: partial |x|^2 and x.g of the four warpgroups
 };
-static_assert(sizeof(Barriers) <= 12288, "barrier block too large");
+static_assert(sizeof(Barriers) <= 16384, "barrier block too large");
 
 // Bounded wait on an mbarrier phase; with honour_abort it also gives up as
 // soon as another role of the CTA has raised the abort flag.
@@ -320,6 +326,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
         ptx::mbar_init(ptx::smem_u32(&bars->acc_full), 1);
         ptx::mbar_init(ptx::smem_u32(&bars->acc_free), kMathThreads);
         ptx::mbar_init(ptx::smem_u32(&bars->red), kMathThreads);
+        ptx::mbar_init(ptx::smem_u32(&bars->fin), kMathThreads);
         for (int s = 0; s < kItemQ; ++s) {
             ptx::mbar_init(ptx::smem_u32(&bars->item_full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->item_empty[s]), T::kItemConsumers);
@@ -649,7 +656,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                prm.err, kDbgTmem);
         const uint32_t s_full = ptx::smem_u32(&bars->s_full), s_free = ptx::smem_u32(&bars->s_free);
         const uint32_t a_full = ptx::smem_u32(&bars->a_full), a_free = ptx::smem_u32(&bars->a_free);
-        uint32_t sf_phase = 0, af_phase = 0, accf_phase = 0, red_phase = 0, qi = 0, ring_idx = 0;
+        uint32_t sf_phase = 0, af_phase = 0, accf_phase = 0, red_phase = 0, fin_phase = 0, qi = 0, ring_idx = 0;
         bool a_pending = false;
         const float log2e = 1.4426950408889634f;
         int pe = is_reweight(MODE) ? prm.p : 1;   // this item's exponent (per head when asked)
@@ -686,6 +693,72 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
             ptx::tc_fence_before();
             ptx::mbar_arrive(a_full);
             a_pending = true;
+            return true;
+        };
+        // The gradient of the L2 row normalisation x -> x / max(|x|, 1e-12)
+        // of this thread's anchor row (q in the row pass, k in the column
+        // pass), from gv, this warpgroup's D/4 columns of the gradient with
+        // respect to the normalised row: y = (g - x (x.g) / |x|^2) / |x| for
+        // |x| > 1e-12 (else g / 1e-12) in the normalised modes, y = g in the
+        // softmax modes.  |x|^2 and x.g span the whole row, whose columns lie
+        // in the four warpgroups, so their partial sums meet in shared memory
+        // at a bounded mbarrier (every math thread arrives, also past L).
+        auto finish_row = [&](const float (&gv)[D / 4], int bh, int arow, bool valid) -> bool {
+            constexpr int Q = D / 4;
+            const size_t off = ((size_t)bh * prm.L + arow) * D + g * Q;
+            const bool live = valid && dcheck(bh < prm.BH && arow < prm.L, prm.err, kDbgGlobal);
+            float y[Q];
+            if constexpr (uses_normalised_qk(MODE)) {
+                float xv[Q];
+                float ss = 0.f, dot = 0.f;
+#pragma unroll
+                for (int c = 0; c < Q / 8; ++c) {
+                    uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                    if (live) u = *reinterpret_cast<const uint4 *>(prm.xraw + off + 8 * c);
+                    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(h[e]);
+                        xv[8 * c + 2 * e] = f.x;
+                        xv[8 * c + 2 * e + 1] = f.y;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < Q; ++e) {
+                    ss = fmaf(xv[e], xv[e], ss);
+                    dot = fmaf(xv[e], gv[e], dot);
+                }
+                bars->x_fin[0][g][t] = ss;
+                bars->x_fin[1][g][t] = dot;
+                ptx::mbar_arrive(ptx::smem_u32(&bars->fin));
+                if (!wait_warp(ptx::smem_u32(&bars->fin), fin_phase, kErrFin)) return false;
+                fin_phase ^= 1;
+                ss = (bars->x_fin[0][0][t] + bars->x_fin[0][1][t]) + (bars->x_fin[0][2][t] + bars->x_fin[0][3][t]);
+                dot = (bars->x_fin[1][0][t] + bars->x_fin[1][1][t]) + (bars->x_fin[1][2][t] + bars->x_fin[1][3][t]);
+                const float n = sqrtf(ss);
+                if (n > 1e-12f) {
+                    const float inv = 1.f / n, radial = dot * inv * inv;
+#pragma unroll
+                    for (int e = 0; e < Q; ++e) y[e] = (gv[e] - xv[e] * radial) * inv;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < Q; ++e) y[e] = gv[e] * 1e12f;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < Q; ++e) y[e] = gv[e];
+            }
+            if (live) {
+#pragma unroll
+                for (int c = 0; c < Q / 8; ++c) {
+                    uint4 u;
+                    u.x = ptx::pack_bf16x2(y[8 * c], y[8 * c + 1]);
+                    u.y = ptx::pack_bf16x2(y[8 * c + 2], y[8 * c + 3]);
+                    u.z = ptx::pack_bf16x2(y[8 * c + 4], y[8 * c + 5]);
+                    u.w = ptx::pack_bf16x2(y[8 * c + 6], y[8 * c + 7]);
+                    *reinterpret_cast<uint4 *>(prm.grad + off + 8 * c) = u;
+                }
+            }
             return true;
         };
         bool ok = true;
@@ -814,7 +887,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                     if (!(ok = store_a(w1, w1))) break;
                 }
                 if (!ok) break;
-                // epilogue: dqh = r * Acc1, this warpgroup's D/4 columns
+                // epilogue: dq from dqh = r * Acc1, this warpgroup's D/4 columns
                 if (!(ok = wait_warp(ptx::smem_u32(&bars->acc_full), accf_phase, kErrAccFull))) break;
                 accf_phase ^= 1;
                 ptx::tc_fence_after();
@@ -830,13 +903,10 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ptx::smem_u32(&bars->acc_free));
-                if (valid && dcheck(bh < prm.BH && arow < prm.L, prm.err, kDbgGlobal)) {
-                    float4 *dst = reinterpret_cast<float4 *>(prm.acc_out + ((size_t)bh * prm.L + arow) * D + g * (D / 4));
+                float gv[D / 4];
 #pragma unroll
-                    for (int c = 0; c < D / 16; ++c)
-                        dst[c] = make_float4(__uint_as_float(acc[4 * c]) * r, __uint_as_float(acc[4 * c + 1]) * r,
-                                             __uint_as_float(acc[4 * c + 2]) * r, __uint_as_float(acc[4 * c + 3]) * r);
-                }
+                for (int e = 0; e < D / 4; ++e) gv[e] = __uint_as_float(acc[e]) * r;
+                if (!(ok = finish_row(gv, bh, arow, valid))) break;
             } else {
                 // ---------------- column pass: key row arow, query tiles at..n_tiles-1
                 const float R = __uint_as_float(prm.rmax[bh]);
@@ -948,7 +1018,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                     a_pending = true;
                 }
                 if (!ok) break;
-                // epilogue: dkh = R * Acc1, dv = Acc2
+                // epilogue: dv = Acc2, and dk from dkh = R * Acc1
                 if (!(ok = wait_warp(ptx::smem_u32(&bars->acc_full), accf_phase, kErrAccFull))) break;
                 accf_phase ^= 1;
                 ptx::tc_fence_after();
@@ -967,12 +1037,7 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                 ptx::mbar_arrive(ptx::smem_u32(&bars->acc_free));
                 if (valid && dcheck(bh < prm.BH && arow < prm.L, prm.err, kDbgGlobal)) {
                     const size_t off = ((size_t)bh * prm.L + arow) * D + g * (D / 4);
-                    float4 *dst = reinterpret_cast<float4 *>(prm.acc_out + off);
                     uint4 *dvd = reinterpret_cast<uint4 *>(prm.dv + off);
-#pragma unroll
-                    for (int c = 0; c < D / 16; ++c)
-                        dst[c] = make_float4(__uint_as_float(acc[4 * c]) * R, __uint_as_float(acc[4 * c + 1]) * R,
-                                             __uint_as_float(acc[4 * c + 2]) * R, __uint_as_float(acc[4 * c + 3]) * R);
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         const uint32_t *q8 = &acc2[8 * c];
@@ -984,6 +1049,10 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
                         dvd[c] = u;
                     }
                 }
+                float gv[D / 4];
+#pragma unroll
+                for (int e = 0; e < D / 4; ++e) gv[e] = __uint_as_float(acc[e]) * R;
+                if (!(ok = finish_row(gv, bh, arow, valid))) break;
             }
         }
     }
