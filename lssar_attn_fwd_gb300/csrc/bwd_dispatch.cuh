@@ -27,8 +27,20 @@ cudaError_t launch_kernel(const Maps &m, const Params &prm, int grid, cudaStream
         return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     });
     if (e != cudaSuccess) return e;
-    kern<<<grid, Tmem<D, PASS>::kThreads, smem, stream>>>(m.x1, m.x2, m.y1, m.y2, prm);
-    return cudaGetLastError();
+    // a programmatic dependent of the kernel before it (the prologue, or the
+    // row pass for the column pass): the launch and the kernel's setup overlap
+    // that kernel's tail (the kernel waits before it reads anything)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Tmem<D, PASS>::kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, m.x1, m.x2, m.y1, m.y2, prm);
 }
 
 // Re-weighting modes: fixed power chains for p = 3 and 15, square-and-multiply otherwise.

@@ -343,6 +343,13 @@ lssar_bwd_kernel(const __grid_constant__ CUtensorMap tmX1, const __grid_constant
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // The launch may overlap the kernel before it (a programmatic dependent
+    // launch): everything above is local setup; what earlier work wrote (the
+    // normalised rows, the zeroed counters, the row pass's records) is read
+    // only after this.  The row pass then lets the column pass launch: its
+    // CTAs take an SM as this pass's CTAs leave, and wait here in turn.
+    ptx::grid_dependency_wait();
+    if constexpr (kRow) ptx::launch_dependents();
 
     const int BH = prm.BH;
     // item -> head, anchor tile, partner tiles [p0, p1); longest items first
