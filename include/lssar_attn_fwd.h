@@ -221,7 +221,11 @@ int lssar_attn_fwd_simt(const void *q, const void *k, const void *v, void *out,
  * `ev_main` just before the attention kernel and `ev_end` after it.  Any event
  * may be NULL (not recorded).  Events are created and owned by the caller.
  * Used by the benchmark to time the attention kernel alone; the computation
- * is identical to lssar_attn_fwd.
+ * is identical to lssar_attn_fwd.  A non-NULL ev_main costs time: the
+ * attention kernel is launched as a programmatic dependent of the prologue
+ * (its launch and setup overlap the prologue's tail), and an event recorded
+ * between the two makes it wait for the prologue to finish first (about 5 us
+ * per call on GB300).
  */
 int lssar_attn_fwd_profiled(const void *q, const void *k, const void *v, void *out,
                             int B, int H, int L, int d, int p, int mode, cudaStream_t stream,

@@ -354,14 +354,13 @@ def lssar_attn_decode(q, k_cache, v_cache, p=3, mode=MODE_LSSAR, out=None, strea
 def lssar_attn_fwd_profiled(q, k, v, p, mode, out, stream, ev_start, ev_main, ev_end):
     """The tensor-core forward recording caller-owned torch.cuda.Events around
     the prologue and the attention kernel (each event must have been recorded
-    once before, so that its CUDA handle exists)."""
+    once before, so that its CUDA handle exists; None skips that event)."""
     B, H, L, d = q.shape
+    handle = lambda e: ctypes.c_void_p(None if e is None else e.cuda_event)  # noqa: E731
     status = load_library().lssar_attn_fwd_profiled(
         ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
         ctypes.c_void_p(out.data_ptr()), B, H, L, d, int(p), int(mode),
-        ctypes.c_void_p(stream.cuda_stream),
-        ctypes.c_void_p(ev_start.cuda_event), ctypes.c_void_p(ev_main.cuda_event),
-        ctypes.c_void_p(ev_end.cuda_event))
+        ctypes.c_void_p(stream.cuda_stream), handle(ev_start), handle(ev_main), handle(ev_end))
     _check(status)
     return out
 
