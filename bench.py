@@ -39,7 +39,8 @@ FLUSH_BYTES = 256 << 20
 L2_BYTES = 129 << 20   # GB300 L2
 FALLBACK_BF16_TFLOPS = 1900.0
 SPEC_DENSE_BF16_TFLOPS = 2250.0   # GB300 nominal dense bf16 tensor peak (context beside the measured one)
-MIN_LOAD_S = 0.6                  # seconds of the same step under load for the clock record
+MIN_LOAD_S = 1.5                  # seconds of the same step under load for the clock record (nvidia-smi
+                                  # averages utilisation over up to a second)
 
 
 def gemm_count(mode):
@@ -96,6 +97,18 @@ def kernel_traffic(workload, mode, p):
     except Exception:
         pass
     return None
+
+
+def hold_load(step, seconds):
+    """Untimed repeats of one step (synchronised every 20 calls) until the GPU
+    has run it for `seconds`, so that the clock record holds samples taken
+    under load also when the timed region is short."""
+    import torch
+    t = time.time()
+    while time.time() - t < seconds:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
 
 
 class ClockSampler:
@@ -533,6 +546,14 @@ def run_decode(args, mode, p):
     torch.cuda.synchronize()
     t1 = time.time()
     sampler.query_once()
+
+    def step():
+        if flush_each:
+            flush.zero_()
+        api.lssar_attn_decode(q, k, v, p=p, mode=mode, out=out)
+    hold_load(step, MIN_LOAD_S)
+    t2 = time.time()
+    sampler.query_once()
     sampler.stop()
     ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
     gbs = cache_bytes / (ms * 1e-3) / 1e9
@@ -550,7 +571,7 @@ def run_decode(args, mode, p):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": f"{kind} hbm_gbs"},
         "plan": plan,
-        "clocks": sampler.summary(t0 - 1.0, t1 + 1.0, timed=(t0, t1)),
+        "clocks": sampler.summary(t0, t2, timed=(t0, t1)),
         "gpu_launches": plan["launches"] * args.steps}), flush=True)
 
 
@@ -591,6 +612,13 @@ def run_backward(args, wl, mode, p):
     torch.cuda.synchronize()
     t1 = time.time()
     sampler.query_once()
+
+    def step():
+        flush.zero_()
+        api.lssar_attn_bwd(q, k, v, dout, stats, p=p, mode=mode)
+    hold_load(step, MIN_LOAD_S)
+    t2 = time.time()
+    sampler.query_once()
     sampler.stop()
     assert api.device_error_word() == 0
     ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
@@ -606,7 +634,7 @@ def run_backward(args, wl, mode, p):
                    "l2": "flushed before every step (256 MiB write)"},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "peak_source": f"{kind} bf16_tflops (burst)"},
-        "clocks": sampler.summary(t0 - 1.0, t1 + 1.0, timed=(t0, t1)),
+        "clocks": sampler.summary(t0, t2, timed=(t0, t1)),
         "gpu_launches": (4 if uses_normalised(mode) else 3) * args.steps}), flush=True)
 
 

@@ -40,3 +40,18 @@ def test_forward_bench_line_has_the_contract_keys():
     assert d["clocks"]["samples"] >= 2 and d["clocks"]["samples_timed"] >= 2
     assert d["clocks"]["samples_under_load"] >= 1 and d["clocks"]["sm_mhz"] is not None
     assert abs(d["pct_bf16_spec_peak"] - 100.0 * d["value"] / 2250.0) < 1e-6
+
+
+@pytest.mark.parametrize("leg", ["--backward", "--decode"])
+def test_backward_and_decode_lines_have_a_clock_record(leg):
+    # the backward and decode legs also hold the same step under load after
+    # their (here very short) timed region, so that their clock record has
+    # samples taken under load
+    r = subprocess.run([sys.executable, "bench.py", leg, "--steps", "5", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    c = d["clocks"]
+    assert c["samples"] >= 2 and c["samples_timed"] >= 2
+    assert c["samples_under_load"] >= 1 and c["sm_mhz"] is not None
