@@ -128,11 +128,13 @@ int lssar_attn_fwd_train(const void *q, const void *k, const void *v, void *out,
  * Same operation, arguments, results and errors as lssar_attn_bwd_simt below.
  * Two persistent tcgen05 kernels: a pass over each 128-query tile (dq, and the
  * per-query terms D_i = dout_i . out_i and the re-weighting threshold's
- * gradient) and a pass over each 128-key tile (dk, dv); scores use fp16
- * normalised rows as in the forward, the gradient products fp16 (normalised
- * modes) or bf16 (softmax modes) with fp32 accumulation.  Scratch:
- * 256 + 4*B*H + 4*B*H*L*d (normalised modes) + 32*B*H*ceil(L/128)*128 +
- * 8*B*H*L*d bytes from the library's stream-ordered pool.
+ * gradient) and a pass over each 128-key tile (dk, dv), each applying the
+ * gradient of the L2 row normalisation to its own tile before it writes;
+ * scores use fp16 normalised rows as in the forward, the gradient products
+ * fp16 (normalised modes) or bf16 (softmax modes) with fp32 accumulation.
+ * Scratch: 256 + round_up(4*B*H, 256) + 2*round_up(2*B*H*L*d, 256)
+ * (normalised modes only) + round_up(32*B*H*ceil(L/128)*128, 256) bytes from
+ * the library's stream-ordered pool.
  */
 int lssar_attn_bwd(const void *q, const void *k, const void *v, const void *dout,
                    const float *stats, void *dq, void *dk, void *dv,
