@@ -635,7 +635,7 @@ def run_backward(args, wl, mode, p):
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "peak_source": f"{kind} bf16_tflops (burst)"},
         "clocks": sampler.summary(t0, t2, timed=(t0, t1)),
-        "gpu_launches": (4 if uses_normalised(mode) else 3) * args.steps}), flush=True)
+        "gpu_launches": (3 if uses_normalised(mode) else 2) * args.steps}), flush=True)   # prologue, row, column pass
 
 
 def uses_normalised(mode):
