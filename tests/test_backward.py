@@ -379,3 +379,46 @@ def test_backward_tc_one_exponential_weights(torch_mod, p, monkeypatch):
     ref = reference(qb, kb, vb, db, MODE_LSSAR, p)
     assert_close(got_f, ref, MODE_LSSAR, p, "one-exponential")
     assert_close(got_e, ref, MODE_LSSAR, p, "exact")
+
+
+@pytest.mark.parametrize("mode,p", [(MODE_LSSAR, 3), (MODE_LSSAR, 15), (MODE_SOFTMAX, 1), (MODE_SIGMOID_RW, 3)])
+def test_backward_tc_zero_rows(torch_mod, mode, p):
+    # All-zero query and key rows: the L2 normalisation max(|x|, 1e-12) takes
+    # its floor there (zero scores: the query row is uniform, in LSSAR the
+    # 0/0 prefix-mean row of the notes' re-weighting), and the fused
+    # normalisation gradient of both passes takes its |x| <= 1e-12 branch.
+    # In the normalised modes a zero key row's dk is its gradient with respect
+    # to the normalised row times 1e12: those rows are checked against the
+    # oracle each on its own scale, every other element with the usual bar.
+    from lssar_attn_fwd_gb300 import api
+    torch = torch_mod
+    B, H, L, d = 1, 2, 300, 64
+    zq, zk = [4, 76, 199], [9, 149]
+    qb, kb, vb = make_qkv(B, H, L, d, seed=41 + mode)
+    qb[:, :, zq] = 0           # bf16 +0.0 is the all-zero bit pattern
+    kb[:, :, zk] = 0
+    d0 = make_dout(B, H, L, d, seed=41 + mode)
+    db = well_conditioned_dout(qb, kb, d0, mode, p)
+    dropped = int(np.any(db != d0, axis=-1).sum())
+    assert dropped <= max(1, MAX_DROPPED * B * H * L), dropped
+    q, k, v, dout = (to_dev(torch, t) for t in (qb, kb, vb, db))
+    out, stats = api.lssar_attn_fwd_train(q, k, v, p=p, mode=mode)
+    grads = api.lssar_attn_bwd(q, k, v, dout, stats, p=p, mode=mode)
+    torch.cuda.synchronize()
+    assert api.device_error_word() == 0
+    ref_out = attention_forward(*(bf16_bits_to_f64(t) for t in (qb, kb, vb)), mode, p)
+    assert np.abs(to_np(out) - ref_out).max() <= tol(mode, p)
+    got = [to_np(t) for t in grads]
+    ref = list(reference(qb, kb, vb, db, mode, p))
+    assert all(np.isfinite(g).all() for g in got)
+    t = tol(mode, p)
+    g_rows, r_rows = got[1][:, :, zk], ref[1][:, :, zk]
+    scale = np.abs(r_rows).max(axis=-1, keepdims=True)
+    assert (np.abs(g_rows - r_rows) <= t * scale + 2.0 ** -8 * np.abs(r_rows)).all()
+    got[1][:, :, zk] = 0.0
+    ref[1][:, :, zk] = 0.0
+    if mode != MODE_SOFTMAX:
+        # a zero query row reads as uniform (LSSA) or as the 0/0 row (LSSAR,
+        # sigmoid re-weighting): its scores get no gradient, so neither does q
+        assert np.abs(got[0][:, :, zq]).max() == 0.0
+    assert_close(tuple(got), tuple(ref), mode, p, "zero rows")
