@@ -300,12 +300,11 @@ def config_dict(wl, mode, p):
 def run_ours(args, wl, mode, p):
     import torch
     ws, rank, local = dist_env()
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)   # each rank's GPU before any CUDA work or communicator
     if ws > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
-        torch.cuda.set_device(local)
-    dev = torch.device("cuda", local if ws > 1 else 0)
-    torch.cuda.set_device(dev)
+        dist.init_process_group("nccl", device_id=dev)
     from lssar_attn_fwd_gb300 import api
     from lssar_attn_fwd_gb300.build import build
     if rank == 0:
